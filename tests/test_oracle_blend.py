@@ -1,0 +1,105 @@
+"""Pins of the oracle's whole layer: the fused cache definition, the r = 100% identity
+and the gradual filter's structure, on the seeded workloads."""
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from oracle.blend import blend_layer, blend_request, gradual_filter_schedule
+from oracle.deviation import bf16_bits_to_f64
+from oracle.rope import rerotate, rope_rotate, round_bf16
+from oracle.topk import k_for_ratio
+from workloads import get_config
+from workloads.generator import generate_layer
+
+
+def _small_multilayer():
+    # Mistral-like structure at a size the oracle runs in seconds: 4 chunks x 64 + 16,
+    # 8 q / 2 kv heads, 4 layers, r1 = 30% -> r2 = 15%.
+    base = get_config("mistral7b")
+    return dataclasses.replace(base, name="small4", config_id=90, n_chunks=4, chunk_len=64,
+                               n_suffix=16, hq=8, hkv=2, head_dim=64, layers=4)
+
+
+def test_fused_cache_is_new_on_selection_and_old_elsewhere():
+    cfg = get_config("tiny")
+    inp = generate_layer(cfg, 1)
+    k = k_for_ratio(cfg.r1_pct, cfg.n_ctx)
+    res = blend_layer(cfg, inp, 1, np.arange(cfg.n_ctx), k, True, attention_rows=False)
+    n_ctx, n = cfg.n_ctx, cfg.n_tokens
+    assert res.sel_tok.size == k and np.all(np.diff(res.sel_tok) > 0)
+    p_new = np.arange(n)
+    p_old = np.arange(n_ctx) % cfg.chunk_len
+    old_rot = round_bf16(rerotate(bf16_bits_to_f64(inp.k_old), p_old, p_new[:n_ctx], cfg.rope_theta))
+    new_enc = round_bf16(rope_rotate(bf16_bits_to_f64(inp.k_new), p_new, cfg.rope_theta))
+    is_new = np.zeros(n, bool)
+    is_new[res.sel_tok] = True
+    is_new[n_ctx:] = True
+    assert np.array_equal(res.is_new, is_new)
+    for t in range(n):
+        if is_new[t]:
+            assert np.array_equal(res.k_fused[t], new_enc[t])
+            assert np.array_equal(res.v_fused[t], bf16_bits_to_f64(inp.v_new[t]))
+        else:
+            assert np.array_equal(res.k_fused[t], old_rot[t])
+            assert np.array_equal(res.v_fused[t], bf16_bits_to_f64(inp.v_old[t]))
+    # chunk 0 keys are not moved (delta 0): bitwise the cached bytes
+    first = ~is_new[: cfg.chunk_len]
+    assert np.array_equal(res.k_fused[: cfg.chunk_len][first], bf16_bits_to_f64(inp.k_old[: cfg.chunk_len])[first])
+
+
+def test_full_ratio_equals_full_recompute_attention():
+    # "数学推导" §形式化: with S = every token, Attention(Q, K_fused, V_fused) is
+    # Attention(Q, K_new, V_new). Checked against torch's causal attention.
+    cfg = get_config("tiny").with_ratio(100)
+    inp = generate_layer(cfg, 1)
+    res = blend_layer(cfg, inp, 1, np.arange(cfg.n_ctx), cfg.n_ctx, True)
+    n = cfg.n_tokens
+    assert res.q_tok.tolist() == list(range(n))
+    pos = np.arange(n)
+    q = round_bf16(rope_rotate(bf16_bits_to_f64(inp.q), pos, cfg.rope_theta))
+    k = round_bf16(rope_rotate(bf16_bits_to_f64(inp.k_new), pos, cfg.rope_theta))
+    v = bf16_bits_to_f64(inp.v_new)
+    g = cfg.hq // cfg.hkv
+    t = lambda x, rep: torch.from_numpy(np.repeat(x, rep, axis=1)).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q, 1), t(k, g), t(v, g), is_causal=True)
+    np.testing.assert_allclose(res.out, ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_selection_finds_the_high_deviation_tokens():
+    # With sigma 1.0 on 15% of tokens and 0.01 elsewhere, the r = 15% selection is
+    # exactly the noisy set (the deviation gap is ~10^4).
+    cfg = get_config("tiny")
+    inp = generate_layer(cfg, 1)
+    res = blend_layer(cfg, inp, 1, np.arange(cfg.n_ctx), k_for_ratio(15, cfg.n_ctx), True, attention_rows=False)
+    assert set(res.sel_tok.tolist()) == set(inp.hkvd_set.tolist())
+
+
+def test_gradual_filter_structure_over_layers():
+    cfg = _small_multilayer()
+    from workloads.generator import hkvd_noise_sets
+    sets = hkvd_noise_sets(cfg)
+    inputs = (generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1))
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
+    prev = None
+    results = list(blend_request(cfg, inputs, attention_rows=False))
+    for (layer, k, selects), res in zip(sched, results):
+        assert res.sel_tok.size == k
+        assert set(res.sel_tok.tolist()) <= set(res.cand.tolist())
+        assert np.array_equal(res.cand[res.sel_row], res.sel_tok)
+        if prev is not None:
+            assert np.array_equal(res.cand, prev.sel_tok)
+        if not selects:
+            assert res.dev is None and np.array_equal(res.sel_tok, prev.sel_tok)
+        prev = res
+    assert results[0].cand.size == cfg.n_ctx
+
+
+def test_workload_generator_is_deterministic_and_shaped():
+    cfg = get_config("tiny")
+    a, b = generate_layer(cfg, 1), generate_layer(cfg, 1)
+    for f in ("k_old", "v_old", "k_new", "v_new", "q"):
+        assert np.array_equal(getattr(a, f), getattr(b, f))
+    assert a.k_old.shape == (512, 2, 64) and a.k_new.shape == (544, 2, 64) and a.q.shape == (544, 4, 64)
+    assert a.hkvd_set.size == 76

@@ -1,0 +1,121 @@
+"""Seeded input generator: the bytes both the CUDA path and the oracle consume.
+
+Every tensor is drawn in fp32 from numpy's PCG64 and rounded once to bf16
+(round to nearest, ties to even); arrays hold raw bf16 bit patterns as uint16.
+Streams are keyed by (workload seed, layer, tensor id), so any one layer can be
+regenerated alone.
+
+What is drawn, per layer (the input recipe):
+  k_old, v_old   [n_ctx, hkv, d]    ~ N(0, 1)   the reused chunk caches
+  k_new, v_new   [n_tokens, hkv, d] token-indexed recomputed K (before RoPE)
+                                    and V. Context rows: old + s_t * eps with
+                                    eps ~ N(0, 1); suffix rows: fresh N(0, 1)
+  q              [n_tokens, hq, d]  ~ N(0, 1), before RoPE
+where s_t is the per-token noise scale of the workload: sigma_hi on the
+high-deviation set H_l and sigma_lo elsewhere, or a lognormal scale.
+H_1 is a seeded random subset; H_{l+1} is H_l with a seeded fraction of its
+members swapped for tokens outside it.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from .configs import BlendConfig
+
+_T_K_OLD, _T_V_OLD, _T_K_EPS, _T_V_EPS, _T_Q = 0, 1, 2, 3, 4
+_T_K_SUF, _T_V_SUF, _T_LOGN, _T_SETS = 5, 6, 7, 100
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to fp32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _rng(cfg: BlendConfig, layer: int, tensor: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([cfg.seed, layer, tensor])))
+
+
+def hkvd_noise_sets(cfg: BlendConfig) -> list:
+    """Per-layer high-deviation token sets H_1 .. H_layers (sorted int64 arrays).
+
+    Empty list entries never occur for the "set" noise model; the lognormal
+    model has no set and returns a list of None.
+    """
+    if cfg.noise != "set":
+        return [None] * cfg.layers
+    rng = _rng(cfg, 0, _T_SETS)
+    size = int(np.floor(cfg.hkvd_frac * cfg.n_ctx))
+    cur = np.sort(rng.choice(cfg.n_ctx, size=size, replace=False)).astype(np.int64)
+    sets = [cur]
+    for _ in range(1, cfg.layers):
+        n_swap = int(np.floor(cfg.swap_frac * cur.size))
+        if n_swap > 0:
+            out = rng.choice(cur, size=n_swap, replace=False)
+            outside = np.setdiff1d(np.arange(cfg.n_ctx, dtype=np.int64), cur, assume_unique=True)
+            inn = rng.choice(outside, size=n_swap, replace=False)
+            cur = np.sort(np.concatenate([np.setdiff1d(cur, out, assume_unique=True), inn]))
+        sets.append(cur)
+    return sets
+
+
+@dataclass
+class LayerInputs:
+    layer: int
+    k_old: np.ndarray        # uint16 bf16 bits [n_ctx, hkv, d]
+    v_old: np.ndarray        # uint16 bf16 bits [n_ctx, hkv, d]
+    k_new: np.ndarray        # uint16 bf16 bits [n_tokens, hkv, d]
+    v_new: np.ndarray        # uint16 bf16 bits [n_tokens, hkv, d]
+    q: np.ndarray            # uint16 bf16 bits [n_tokens, hq, d]
+    noise_scale: np.ndarray  # float32 [n_ctx]
+    hkvd_set: np.ndarray | None
+
+
+def noise_scales(cfg: BlendConfig, layer: int, hset) -> np.ndarray:
+    if cfg.noise == "set":
+        s = np.full(cfg.n_ctx, cfg.sigma_lo, dtype=np.float32)
+        s[hset] = cfg.sigma_hi
+        return s
+    if cfg.noise == "lognormal":
+        z = _rng(cfg, layer, _T_LOGN).standard_normal(cfg.n_ctx, dtype=np.float32)
+        return np.exp(np.float32(cfg.lognormal_mu) + np.float32(cfg.lognormal_sigma) * z).astype(np.float32)
+    raise ValueError(f"unknown noise model {cfg.noise!r}")
+
+
+def generate_layer(cfg: BlendConfig, layer: int, sets: list | None = None) -> LayerInputs:
+    """Inputs of one layer (1-based). Pass `sets` from hkvd_noise_sets to avoid recomputing it."""
+    if not 1 <= layer <= cfg.layers:
+        raise ValueError(f"layer {layer} outside 1..{cfg.layers}")
+    if sets is None:
+        sets = hkvd_noise_sets(cfg)
+    hset = sets[layer - 1]
+    n_ctx, n, hkv, hq, d = cfg.n_ctx, cfg.n_tokens, cfg.hkv, cfg.hq, cfg.head_dim
+    s = noise_scales(cfg, layer, hset)[:, None, None]
+
+    k_old = f32_to_bf16_bits(_rng(cfg, layer, _T_K_OLD).standard_normal((n_ctx, hkv, d), dtype=np.float32))
+    v_old = f32_to_bf16_bits(_rng(cfg, layer, _T_V_OLD).standard_normal((n_ctx, hkv, d), dtype=np.float32))
+
+    k_new = np.empty((n, hkv, d), dtype=np.uint16)
+    v_new = np.empty((n, hkv, d), dtype=np.uint16)
+    k_eps = _rng(cfg, layer, _T_K_EPS).standard_normal((n_ctx, hkv, d), dtype=np.float32)
+    k_new[:n_ctx] = f32_to_bf16_bits(bf16_bits_to_f32(k_old) + s * k_eps)
+    del k_eps
+    v_eps = _rng(cfg, layer, _T_V_EPS).standard_normal((n_ctx, hkv, d), dtype=np.float32)
+    v_new[:n_ctx] = f32_to_bf16_bits(bf16_bits_to_f32(v_old) + s * v_eps)
+    del v_eps
+    n_suf = cfg.n_suffix
+    k_new[n_ctx:] = f32_to_bf16_bits(_rng(cfg, layer, _T_K_SUF).standard_normal((n_suf, hkv, d), dtype=np.float32))
+    v_new[n_ctx:] = f32_to_bf16_bits(_rng(cfg, layer, _T_V_SUF).standard_normal((n_suf, hkv, d), dtype=np.float32))
+
+    q = f32_to_bf16_bits(_rng(cfg, layer, _T_Q).standard_normal((n, hq, d), dtype=np.float32))
+    return LayerInputs(layer, k_old, v_old, k_new, v_new, q, s[:, 0, 0].copy(), hset)
