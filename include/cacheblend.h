@@ -1,0 +1,198 @@
+/*
+ * cacheblend.h — C ABI of the GB300 (sm_103a) CacheBlend per-layer KV blend.
+ *
+ * CacheBlend reuses KV caches that were computed for each retrieved chunk on
+ * its own. Per transformer layer the blend (1) moves every cached key from its
+ * chunk-local RoPE position to its position in the concatenated request,
+ * (2) scores each candidate token by the squared L2 distance between its
+ * recomputed and its cached V, (3) keeps the k highest-scoring tokens (the
+ * high-KV-deviation, HKVD, tokens) under the gradual filter, (4) splices their
+ * recomputed K/V into the reused cache and (5) runs causal grouped-query
+ * attention for the HKVD tokens and the query suffix over the fused cache.
+ *
+ * Sources (web pages):
+ *   "数学推导" (CacheBlend appendix C, math derivations):
+ *      §RoPE 位置编码的相对位置不变性证明  RoPE rotation R_p, R_m^T R_n = R_{n-m}
+ *      §CacheBlend 中的应用              k_new = R_{p_new - p_old} k_old
+ *      §问题定义 / §形式化                old/new KV in R^{n x d}, budget k, fused KV
+ *      §近似解                           S = TopK_i ||V_new[i] - V_old[i]||_2^2
+ *   "rag的kvcache问题":
+ *      §渐进式过滤机制                    r1% at layer 1, r2% at layer 2, stable set after
+ *      §独立编码                         chunk caches computed independently
+ *      §transformer训练与推理并行计算的差异  causal mask
+ *      §阶段二                           attention rows are independent
+ *
+ * Conventions for every call:
+ *   - Tensors are bf16, row-major [token, head, dim] ("NHD"), contiguous, on
+ *     the current CUDA device; every bf16 tensor pointer must be 16-byte
+ *     aligned. Index arrays are int32 on the device.
+ *   - The caller owns every tensor. The library owns only what a cb_plan holds
+ *     (RoPE cos/sin table, device error word, per-layer scratch); no call
+ *     other than cb_plan_create / cb_plan_destroy allocates or frees memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every compute
+ *     call only enqueues work on it and returns without synchronising.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns CB_ERR_INVALID_ARG (or CB_ERR_UNSUPPORTED) and
+ *     launches nothing. Problems only the device can see (an index out of
+ *     range, an unsorted list, a wait that ran out of time) skip the offending
+ *     work, never fault, and are recorded in the plan's device error word,
+ *     which cb_check() reads.
+ *   - Sizes of 0 are valid and launch nothing.
+ *   - cb_last_error_string() describes the last failure of this thread.
+ */
+#ifndef CACHEBLEND_H
+#define CACHEBLEND_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cb_status {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape: nothing launched */
+  CB_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels implement (e.g. head_dim) */
+  CB_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  CB_ERR_TIMEOUT = 4,      /* a device-side wait gave up (reported by cb_check) */
+  CB_ERR_DEVICE_CHECK = 5  /* a device-side argument check failed (reported by cb_check) */
+} cb_status;
+
+/* Which coordinates of a head form RoPE pair j (the pages do not fix it). */
+typedef enum cb_rope_style {
+  CB_ROPE_HALF = 0,        /* (j, j + D/2): GPT-NeoX / Llama / Mistral layout */
+  CB_ROPE_INTERLEAVED = 1  /* (2j, 2j + 1) */
+} cb_rope_style;
+
+/* One blend request: n_chunks cached chunks of chunk_len tokens (chunk-local
+ * positions 0 .. chunk_len-1), then n_suffix uncached query tokens. Token i of
+ * the request sits at global position i. r1_pct / r2_pct: gradual-filter
+ * ratios in percent of the n_ctx = n_chunks * chunk_len cached tokens. */
+typedef struct cb_config {
+  int32_t n_chunks;
+  int32_t chunk_len;
+  int32_t n_suffix;
+  int32_t hq;          /* query heads */
+  int32_t hkv;         /* kv heads; hq % hkv == 0 and hq / hkv in {1,2,4,8,16} */
+  int32_t head_dim;    /* 64 or 128 */
+  double rope_theta;   /* RoPE base: pair j turns by p * theta^(-2j/D) */
+  int32_t rope_style;  /* cb_rope_style */
+  int32_t r1_pct;      /* layer-1 keep ratio, 0..100 */
+  int32_t r2_pct;      /* keep ratio from layer 2 on, 0..r1_pct */
+} cb_config;
+
+typedef struct cb_plan cb_plan;
+
+/* Create a plan on the current device: copies *cfg, builds the RoPE cos/sin
+ * table for positions 0 .. n_tokens-1 (fp64 angles rounded to fp32) and the
+ * scratch the per-layer driver needs. Synchronous. */
+cb_status cb_plan_create(const cb_config* cfg, cb_plan** out);
+
+/* Free everything the plan owns. Waits for the device first. NULL is a no-op. */
+cb_status cb_plan_destroy(cb_plan* plan);
+
+/* Sizes of layer `layer` (1-based) under the plan's gradual filter:
+ * n_cand = |C_l| (candidates read), k = |S_l| (kept), mq = k + n_suffix
+ * (attention query rows), selects = 1 if the layer runs deviation + top-k.
+ * Layer 1: C = all n_ctx tokens, k = floor(r1 * n_ctx / 100). Layer 2: C = S_1,
+ * k = floor(r2 * n_ctx / 100). Layer >= 3: C = S_{l-1}, kept whole. */
+cb_status cb_layer_sizes(const cb_plan* plan, int32_t layer, int32_t* n_cand, int32_t* k,
+                         int32_t* mq, int32_t* selects);
+
+/* RoPE row rotation ("数学推导" §RoPE 位置编码的相对位置不变性证明 and
+ * §CacheBlend 中的应用):
+ *   out[out_rows ? out_rows[i] : i] = R_{pos_to[i] - (pos_from ? pos_from[i] : 0)} x[in_rows ? in_rows[i] : i]
+ * for i in [0, n). Each row is n_heads x head_dim (the plan's) bf16; math in
+ * fp32 with the plan's cos/sin table. pos_from == NULL encodes at pos_to
+ * (k~ = R_p k); otherwise it re-rotates a key cached at pos_from to pos_to.
+ * |pos_to - pos_from| must be < n_tokens of the plan (else the row is skipped
+ * and CB_ERR_DEVICE_CHECK is recorded). x holds x_rows rows and out holds
+ * out_rows_total rows; a mapped row outside them is skipped and recorded the
+ * same way. pos_to must not be NULL. out may equal x only when in_rows and
+ * out_rows are both NULL (in place). */
+cb_status cb_rope_rerotate(cb_plan* plan, void* out, const void* x, const int32_t* in_rows,
+                           const int32_t* out_rows, const int32_t* pos_from, const int32_t* pos_to,
+                           int32_t n, int32_t n_heads, int32_t x_rows, int32_t out_rows_total,
+                           void* stream);
+
+/* V deviation ("数学推导" §近似解): for i in [0, m),
+ *   dev[i] = sum_{h, j} (v_new[t, h, j] - v_old[t, h, j])^2,  t = cand ? cand[i] : i,
+ * in fp32 in one fixed order (8-element chunks dealt to 32 lanes, sequential
+ * per lane, then a xor butterfly over lanes 16, 8, 4, 2, 1; products and sums
+ * rounded separately, no fused multiply-add), so the value is reproducible
+ * bit for bit. v_new and v_old are indexed by token ([>= t+1, hkv, D]).
+ * Candidates outside [0, n_ctx) are skipped (dev = NaN, CB_ERR_DEVICE_CHECK). */
+cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, const int32_t* cand,
+                          int32_t m, float* dev, void* stream);
+
+/* HKVD top-k ("数学推导" §近似解; gradual filter of "rag的kvcache问题"
+ * §渐进式过滤机制): keep the k of m candidates with the largest dev, ties to
+ * the lower token id. cand (NULL = identity) must be strictly ascending.
+ * Writes sel_tok[k] (ascending token ids) and sel_row[k] (their indices in
+ * cand). dev values must not be NaN. One thread block; no scratch memory. */
+cb_status cb_hkvd_topk(cb_plan* plan, const float* dev, const int32_t* cand, int32_t m, int32_t k,
+                       int32_t* sel_tok, int32_t* sel_row, void* stream);
+
+/* Fuse / scatter ("数学推导" §形式化): for each token t of sel_tok[0..k) and
+ * each suffix token t in [n_ctx, n_tokens):
+ *   k_fused[t] = R_t k_new[t],  v_fused[t] = v_new[t]
+ * leaving every other row of k_fused / v_fused untouched. k_new / v_new are
+ * token-indexed [n_tokens, hkv, D]; k_fused / v_fused are [n_tokens, hkv, D].
+ * sel_tok must be strictly ascending context token ids. */
+cb_status cb_fuse_scatter(cb_plan* plan, void* k_fused, void* v_fused, const void* k_new,
+                          const void* v_new, const int32_t* sel_tok, int32_t k, void* stream);
+
+/* HKVD causal GQA attention ("数学推导" §形式化; causal mask of
+ * "rag的kvcache问题" §transformer训练与推理并行计算的差异):
+ *   out[i, h] = sum_{j <= q_pos[i]} softmax_j(scale * q[i, h] . k[j, g]) v[j, g],  g = h / (hq/hkv)
+ * q, out: [mq, hq, D] compact query rows already RoPE-encoded at q_pos;
+ * k, v: [n_keys, hkv, D], key j at position j. q_pos strictly ascending,
+ * each < n_keys (a violation is recorded, rows still bounded). scale <= 0
+ * selects 1/sqrt(D). fp32 accumulation and softmax, bf16 P, bf16 output.
+ * tcgen05 (TMEM accumulators) fed by TMA. */
+cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq,
+                            const void* k, const void* v, int32_t n_keys, float scale, void* out,
+                            void* stream);
+
+/* Buffers of one layer for cb_blend_layer. Sizes from cb_layer_sizes. */
+typedef struct cb_layer_io {
+  const void* k_old;     /* [n_ctx, hkv, D] cached keys, at chunk-local positions */
+  const void* v_old;     /* [n_ctx, hkv, D] cached values */
+  const void* k_new;     /* [n_tokens, hkv, D] recomputed keys before RoPE, by token; rows of C_l and the suffix are read */
+  const void* v_new;     /* [n_tokens, hkv, D] recomputed values, by token; same rows */
+  const void* q;         /* [n_tokens, hq, D] queries before RoPE, by token; rows of S_l and the suffix are read */
+  const int32_t* cand;   /* C_l, strictly ascending: NULL at layer 1 (all context tokens), else S_{l-1} */
+  float* dev;            /* [n_cand] out at selecting layers: deviation per candidate (may be NULL otherwise) */
+  int32_t* sel_tok;      /* [k] out: S_l, ascending token ids */
+  int32_t* sel_row;      /* [k] out: rows of S_l in C_l */
+  void* k_fused;         /* [n_tokens, hkv, D] out: fused keys at global positions */
+  void* v_fused;         /* [n_tokens, hkv, D] out: fused values */
+  void* q_rot;           /* [mq, hq, D] out: encoded query rows (S_l, then the suffix) */
+  void* out;             /* [mq, hq, D] out: attention output rows, same order */
+} cb_layer_io;
+
+/* One layer of the blend (1-based `layer`), all on `stream`, no host sync:
+ *   selecting layers: deviation over C_l, then top-k -> S_l;
+ *   other layers:     S_l = C_l;
+ *   then fused K/V for all n_tokens rows in one pass (cached rows re-rotated
+ *   by their chunk offset, S_l and suffix rows encoded from k_new / v_new),
+ *   the query rows encoded, and the attention. */
+cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream);
+
+/* Synchronise the plan's device, read and clear its error word. Returns
+ * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
+ * cb_last_error_string). Off the hot path. */
+cb_status cb_check(cb_plan* plan);
+
+/* Human-readable description of the last failure on this thread. */
+const char* cb_last_error_string(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t cb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CACHEBLEND_H */

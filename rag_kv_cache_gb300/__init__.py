@@ -1,0 +1,160 @@
+"""GB300 (sm_103a) CacheBlend per-layer KV blend.
+
+Thin PyTorch-facing binding of the C ABI in include/cacheblend.h: the same
+call names, tensors passed as device pointers, the current torch stream as
+the CUDA stream. PyTorch only allocates device memory and provides streams;
+every step of the blend runs in the library's CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import CacheBlendError, check
+
+__all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_hkvd_topk", "cb_fuse_scatter",
+           "cb_hkvd_attention", "cb_blend_layer", "cb_check", "cb_version", "LayerBuffers"]
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class Plan:
+    """A cb_plan: one blend request's shapes, RoPE table and scratch on the current device."""
+
+    def __init__(self, n_chunks, chunk_len, n_suffix, hq, hkv, head_dim, rope_theta, rope_style="half",
+                 r1_pct=15, r2_pct=15):
+        lib = _lib.load()
+        self.cfg = _lib.CbConfig(n_chunks, chunk_len, n_suffix, hq, hkv, head_dim, float(rope_theta),
+                                 _lib.ROPE_STYLES[rope_style], r1_pct, r2_pct)
+        self.n_ctx = n_chunks * chunk_len
+        self.n_tokens = self.n_ctx + n_suffix
+        self.hq, self.hkv, self.head_dim = hq, hkv, head_dim
+        self._h = ctypes.c_void_p()
+        check(lib.cb_plan_create(ctypes.byref(self.cfg), ctypes.byref(self._h)))
+
+    @classmethod
+    def from_config(cls, cfg, rope_style="half", r1_pct=None, r2_pct=None):
+        """From a workloads.BlendConfig (or anything with the same fields)."""
+        return cls(cfg.n_chunks, cfg.chunk_len, cfg.n_suffix, cfg.hq, cfg.hkv, cfg.head_dim, cfg.rope_theta,
+                   rope_style, cfg.r1_pct if r1_pct is None else r1_pct, cfg.r2_pct if r2_pct is None else r2_pct)
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise RuntimeError("plan is closed")
+        return self._h
+
+    def layer_sizes(self, layer):
+        v = [ctypes.c_int32() for _ in range(4)]
+        check(_lib.load().cb_layer_sizes(self.handle, layer, *[ctypes.byref(x) for x in v]))
+        return tuple(x.value for x in v)  # (n_cand, k, mq, selects)
+
+    def check(self):
+        check(_lib.load().cb_check(self.handle))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.load().cb_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def cb_version() -> int:
+    return _lib.load().cb_version()
+
+
+def cb_check(plan: Plan) -> None:
+    plan.check()
+
+
+def cb_rope_rerotate(plan, out, x, pos_to, pos_from=None, in_rows=None, out_rows=None, n=None, stream=None):
+    """out[out_rows[i]] = R_{pos_to[i] - pos_from[i]} x[in_rows[i]] (see cacheblend.h)."""
+    n = pos_to.numel() if n is None else n
+    n_heads = x.shape[1]
+    check(_lib.load().cb_rope_rerotate(
+        plan.handle, _ptr(out, torch.bfloat16, "out"), _ptr(x, torch.bfloat16, "x"),
+        _ptr(in_rows, torch.int32, "in_rows"), _ptr(out_rows, torch.int32, "out_rows"),
+        _ptr(pos_from, torch.int32, "pos_from"), _ptr(pos_to, torch.int32, "pos_to"), n, n_heads,
+        x.shape[0], out.shape[0], _stream(stream)))
+
+
+def cb_kv_deviation(plan, v_new, v_old, cand, m, dev, stream=None):
+    check(_lib.load().cb_kv_deviation(
+        plan.handle, _ptr(v_new, torch.bfloat16, "v_new"), _ptr(v_old, torch.bfloat16, "v_old"),
+        _ptr(cand, torch.int32, "cand"), m, _ptr(dev, torch.float32, "dev"), _stream(stream)))
+
+
+def cb_hkvd_topk(plan, dev, cand, m, k, sel_tok, sel_row, stream=None):
+    check(_lib.load().cb_hkvd_topk(
+        plan.handle, _ptr(dev, torch.float32, "dev"), _ptr(cand, torch.int32, "cand"), m, k,
+        _ptr(sel_tok, torch.int32, "sel_tok"), _ptr(sel_row, torch.int32, "sel_row"), _stream(stream)))
+
+
+def cb_fuse_scatter(plan, k_fused, v_fused, k_new, v_new, sel_tok, k, stream=None):
+    check(_lib.load().cb_fuse_scatter(
+        plan.handle, _ptr(k_fused, torch.bfloat16, "k_fused"), _ptr(v_fused, torch.bfloat16, "v_fused"),
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(sel_tok, torch.int32, "sel_tok"), k, _stream(stream)))
+
+
+def cb_hkvd_attention(plan, q, q_pos, mq, k, v, n_keys, out, scale=0.0, stream=None):
+    check(_lib.load().cb_hkvd_attention(
+        plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(q_pos, torch.int32, "q_pos"), mq,
+        _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"), n_keys, float(scale),
+        _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+class LayerBuffers:
+    """Device buffers of one layer's outputs, sized for the plan's largest layer."""
+
+    def __init__(self, plan: Plan, device="cuda"):
+        n1, k1, mq1, _ = plan.layer_sizes(1)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.dev = torch.empty(max(n1, 1), dtype=torch.float32, device=device)
+        self.sel_tok = torch.empty(max(k1, 1), **i32)
+        self.sel_row = torch.empty(max(k1, 1), **i32)
+        self.k_fused = torch.empty(plan.n_tokens, plan.hkv, plan.head_dim, **bf)
+        self.v_fused = torch.empty(plan.n_tokens, plan.hkv, plan.head_dim, **bf)
+        self.q_rot = torch.empty(max(mq1, 1), plan.hq, plan.head_dim, **bf)
+        self.out = torch.empty(max(mq1, 1), plan.hq, plan.head_dim, **bf)
+
+
+def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None):
+    """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer))."""
+    io = _lib.CbLayerIO(
+        _ptr(k_old, torch.bfloat16, "k_old"), _ptr(v_old, torch.bfloat16, "v_old"),
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(cand, torch.int32, "cand"), _ptr(bufs.dev, torch.float32, "dev"),
+        _ptr(bufs.sel_tok, torch.int32, "sel_tok"), _ptr(bufs.sel_row, torch.int32, "sel_row"),
+        _ptr(bufs.k_fused, torch.bfloat16, "k_fused"), _ptr(bufs.v_fused, torch.bfloat16, "v_fused"),
+        _ptr(bufs.q_rot, torch.bfloat16, "q_rot"), _ptr(bufs.out, torch.bfloat16, "out"))
+    check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))

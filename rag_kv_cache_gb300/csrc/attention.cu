@@ -1,0 +1,517 @@
+// HKVD causal grouped-query attention on sm_103a: TMA loads, tcgen05.mma with
+// TMEM accumulators, online softmax with one thread per query row.
+//
+// What it computes ("数学推导" §形式化, the attention over the fused cache;
+// "rag的kvcache问题" §transformer训练与推理并行计算的差异 for the causal mask and
+// §阶段二 for computing only the selected rows):
+//   out[i, h] = sum_{j <= q_pos[i]} softmax_j(scale * q[i, h] . k[j, g]) v[j, g],  g = h / G.
+//
+// Tiling. One CTA owns one kv head g and 128 query rows: TQ = 128 / G query
+// tokens times the G query heads that share g (row r = token r / G, head r % G),
+// so every K/V tile it loads serves all G heads. Key tiles are 128 keys; the
+// CTA visits key tiles 0 .. (largest query position in the tile) / 128.
+//
+// Roles (192 threads):
+//   warps 0-3  softmax + epilogue: thread r owns query row r (TMEM lane r)
+//   warp 4     TMA producer: Q once, then K/V tiles into a 2-stage ring
+//   warp 5     MMA issuer:   S_j = Q K_j^T into TMEM (2 buffers), O += P_j V_j
+// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256 + D).
+// P (bf16) overwrites the first 64 columns of its S buffer and is the A
+// operand of the PV MMA straight from TMEM.
+//
+// Every mbarrier wait is bounded (2 s by the global timer). A wait that gives
+// up records a timeout in the error word, raises a CTA-wide abort flag that
+// ends the other roles' loops, and the CTA drains its tensor-core work and
+// frees its TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tmem_ops.cuh"
+
+namespace cb {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kWarpProducer = 4;
+constexpr int kWarpMma = 5;
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_s(int s) { return s ? 128u : 0u; }
+constexpr uint32_t kColO = 256;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2];
+  uint64_t v_full[2];
+  uint64_t kv_empty[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+};
+
+struct Params {
+  const int32_t* q_pos;
+  int mq;
+  int n_keys;
+  int hq;
+  int hkv;
+  int group;     // query heads per kv head
+  int tq;        // query tokens per tile = 128 / group
+  int n_qtiles;
+  float scale_log2;
+  uint8_t* out;
+  int32_t* err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; false on abort or timeout.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                       int site, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (global_timer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        record_error(err, kErrTimeout, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (8-row x 128-byte atoms).
+// lbo / sbo in bytes: K-major operands use sbo = 1024 (next 8 rows); MN-major
+// operands also use lbo = distance between 64-element blocks of the MN dimension.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for the sm_100 family
+  d |= (uint64_t)2 << 61;  // swizzle: 128 bytes
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, A K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    hkvd_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  constexpr int kBoxes = D / 64;
+  constexpr uint32_t kQBytes = kBM * D * 2;
+  constexpr uint32_t kKVBytes = kBN * D * 2;
+  constexpr uint32_t kQBox = kBM * 128;   // bytes of one 64-column box of Q
+  constexpr uint32_t kKVBox = kBN * 128;  // bytes of one 64-column box of K or V
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_maxpos;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sK[2] = {base + kQBytes, base + kQBytes + kKVBytes};
+  const uint32_t sV[2] = {base + kQBytes + 2 * kKVBytes, base + kQBytes + 3 * kKVBytes};
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int lin = blockIdx.x;
+  const int tile = p.n_qtiles - 1 - lin / p.hkv;  // later (longer) query tiles first
+  const int g = lin % p.hkv;
+  const int t0 = tile * p.tq;
+  const int t_last = min(t0 + p.tq, p.mq) - 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars.q_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.k_full[s]), 1);
+      mbar_init(smem_u32(&bars.v_full[s]), 1);
+      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars.s_full[s]), 1);
+      mbar_init(smem_u32(&bars.p_full[s]), kSoftmaxThreads);
+      mbar_init(smem_u32(&bars.pv_done[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.drain), 1);
+    s_abort = 0;
+    s_maxpos = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+
+  // Each softmax thread's query position; padded rows repeat the tile's last token.
+  int my_pos = 0;
+  if (threadIdx.x < kSoftmaxThreads) {
+    const int r = threadIdx.x;
+    const int t = min(t0 + r / p.group, t_last);
+    int pos = p.q_pos[t];
+    if (pos < 0 || pos >= p.n_keys) {
+      record_error(p.err, kErrIndex, t);
+      pos = pos < 0 ? 0 : p.n_keys - 1;
+    }
+    if (r % p.group == 0 && t == t0 + r / p.group && t > 0 && p.q_pos[t - 1] >= p.q_pos[t])
+      record_error(p.err, kErrOrder, t);
+    my_pos = pos;
+    atomicMax(&s_maxpos, pos);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int n_kv = s_maxpos / kBN + 1;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == kWarpProducer) {
+    if (lane == 0) {
+      const uint32_t qb = smem_u32(&bars.q_full);
+      mbar_expect_tx(qb, kQBytes);
+#pragma unroll
+      for (int b = 0; b < kBoxes; ++b) tma_load_4d(sQ + b * kQBox, &tm_q, qb, b * 64, 0, g, t0);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(smem_u32(&bars.kv_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.err, 1)) break;
+        const uint32_t kb = smem_u32(&bars.k_full[s]), vb = smem_u32(&bars.v_full[s]);
+        mbar_expect_tx(kb, kKVBytes);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b) tma_load_3d(sK[s] + b * kKVBox, &tm_k, kb, b * 64, g, j * kBN);
+        mbar_expect_tx(vb, kKVBytes);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b) tma_load_3d(sV[s] + b * kKVBox, &tm_v, vb, b * 64, g, j * kBN);
+        issued = j + 1;
+      }
+      // Before the CTA can exit, every copy issued must have landed.
+      mbar_wait(qb, 0, abort_flag, p.err, 2, false);
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+        mbar_wait(smem_u32(&bars.k_full[j & 1]), (j >> 1) & 1, abort_flag, p.err, 3, false);
+        mbar_wait(smem_u32(&bars.v_full[j & 1]), (j >> 1) & 1, abort_flag, p.err, 4, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t idesc_o = idesc_bf16(kBM, D, true);
+      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, p.err, 10);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!mbar_wait(smem_u32(&bars.k_full[s]), (j >> 1) & 1, abort_flag, p.err, 11)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int b = ks / 4, kk = ks % 4;
+          const uint64_t a = sdesc(sQ + b * kQBox + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc(sK[s] + b * kKVBox + kk * 32, 16, 1024);
+          mma_ss(tmem + col_s(s), a, bd, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&bars.s_full[s]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j & 1;
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;
+        if (!mbar_wait(smem_u32(&bars.p_full[s]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
+        if (!mbar_wait(smem_u32(&bars.v_full[s]), (j >> 1) & 1, abort_flag, p.err, 13)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t bd = sdesc(sV[s] + ks * 16 * 128, kKVBox, 1024);
+          mma_ts(tmem + kColO, tmem + col_s(s) + ks * 8, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&bars.kv_empty[s]));
+        tc_commit(smem_u32(&bars.pv_done[s]));
+      }
+      // All tensor-core work issued by this CTA completes before TMEM is freed.
+      tc_commit(smem_u32(&bars.drain));
+      mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 14, false);
+    }
+    __syncwarp();
+  } else {
+    const int r = threadIdx.x;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_ref = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1;
+      const bool w = mbar_wait(smem_u32(&bars.s_full[s]), (j >> 1) & 1, abort_flag, p.err, 20);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t raw[128];
+      tmem_ld_x128(lane_base + col_s(s), raw);
+      float x[128];
+      const int kb = j * kBN;
+      const bool need_mask = kb + kBN - 1 > my_pos;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = __uint_as_float(raw[c]) * p.scale_log2;
+        if (need_mask && kb + c > my_pos) v = -INFINITY;
+        x[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      if (j == 0) {
+        m_ref = mx;
+      } else {
+        const bool want = mx > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, want)) {
+          // O holds the sum through tile j-1: wait for that PV, then rescale rows that need it.
+          const bool w2 = mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag, p.err, 21);
+          if (!__all_sync(0xffffffffu, w2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = want ? ex2(m_ref - mx) : 1.0f;
+          if (want) {
+            l *= alpha;
+            m_ref = mx;
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(lane_base + kColO + c0, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_x32(lane_base + kColO + c0, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      float sum = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2(x[h * 64 + 2 * e] - m_ref);
+          const float p1 = ex2(x[h * 64 + 2 * e + 1] - m_ref);
+          sum += p0 + p1;
+          pk[e] = pack2(p0, p1);
+        }
+        tmem_st_x32(lane_base + col_s(s) + h * 32, pk);
+      }
+      tmem_st_wait();
+      l += sum;
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.p_full[s]));
+    }
+    if (ok) {
+      const bool w = mbar_wait(smem_u32(&bars.pv_done[(n_kv - 1) & 1]), ((n_kv - 1) >> 1) & 1, abort_flag, p.err, 22);
+      if (__all_sync(0xffffffffu, w)) {
+        tc_fence_after();
+        const int t = t0 + r / p.group;
+        const bool valid = t <= t_last;
+        const float inv = 1.0f / l;
+        uint8_t* dst = p.out + ((size_t)t * p.hq + (size_t)g * p.group + (r % p.group)) * D * 2;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(lane_base + kColO + c0, o);
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[q * 8 + e]) * inv;
+              *reinterpret_cast<uint4*>(dst + (c0 + q * 8) * 2) = pack8(f);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                const cuuint32_t* box) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void* k, const void* v, int n_keys,
+                         int hq, int hkv, float scale, void* out, int32_t* err, cudaStream_t s) {
+  const int group = hq / hkv;
+  const int tq = kBM / group;
+  const int n_qtiles = (mq + tq - 1) / tq;
+  CUtensorMap tq_map, tk_map, tv_map;
+  const cuuint64_t qd[4] = {(cuuint64_t)D, (cuuint64_t)group, (cuuint64_t)hkv, (cuuint64_t)mq};
+  const cuuint64_t qs[3] = {(cuuint64_t)D * 2, (cuuint64_t)group * D * 2, (cuuint64_t)hq * D * 2};
+  const cuuint32_t qb[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)tq};
+  const cuuint64_t kd[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)n_keys};
+  const cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
+  const cuuint32_t kbx[3] = {64, 1, (cuuint32_t)kBN};
+  if (!encode_map(&tq_map, q, 4, qd, qs, qb) || !encode_map(&tk_map, k, 3, kd, ks, kbx) ||
+      !encode_map(&tv_map, v, 3, kd, ks, kbx))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.q_pos = q_pos;
+  p.mq = mq;
+  p.n_keys = n_keys;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.group = group;
+  p.tq = tq;
+  p.n_qtiles = n_qtiles;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = static_cast<uint8_t*>(out);
+  p.err = err;
+  size_t smem = 1024 + (size_t)(kBM + 4 * kBN) * D * 2;
+  if (smem < 117 * 1024) smem = 117 * 1024;  // one CTA per SM: the CTA takes all 512 TMEM columns
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(hkvd_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  hkvd_attention_kernel<D><<<n_qtiles * hkv, kThreads, smem, s>>>(tq_map, tk_map, tv_map, p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_hkvd_attention(const void* q, const int32_t* q_pos, int32_t mq, const void* k, const void* v,
+                                  int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim, float scale, void* out,
+                                  int32_t* err, cudaStream_t s) {
+  if (mq <= 0) return cudaSuccess;
+  if (head_dim == 128) return launch_typed<128>(q, q_pos, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+  if (head_dim == 64) return launch_typed<64>(q, q_pos, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cb

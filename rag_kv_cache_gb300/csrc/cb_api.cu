@@ -1,0 +1,306 @@
+// C ABI of the blend (declared in include/cacheblend.h): host-side argument
+// checks, the plan (RoPE table, device error word, scratch), and the
+// per-layer driver that enqueues the kernels of one layer on the caller's
+// stream without any host synchronisation.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/cacheblend.h"
+#include "common.cuh"
+#include "kernels.h"
+
+struct cb_plan {
+  cb_config cfg;
+  int device;
+  int32_t n_ctx;
+  int32_t n_tokens;
+  float2* rope_tab;  // [n_tokens][head_dim / 2]
+  int32_t* err;      // [0] flags, [1] first offending index (-1 = none)
+  int32_t* q_pos;    // [n_tokens] positions of the encoded query rows of the current layer
+};
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+cb_status fail(cb_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+cb_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return CB_OK;
+  return fail(CB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cb_status need_tensor(const void* p, const char* name) {
+  if (p == nullptr) return fail(CB_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(CB_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return CB_OK;
+}
+
+cb_status need_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(CB_ERR_INVALID_ARG, "%s is NULL", name);
+  return CB_OK;
+}
+
+#define CB_TRY(expr)                  \
+  do {                                \
+    const cb_status _s = (expr);      \
+    if (_s != CB_OK) return _s;       \
+  } while (0)
+
+cb_status check_plan(const cb_plan* plan) {
+  if (plan == nullptr) return fail(CB_ERR_INVALID_ARG, "plan is NULL");
+  return CB_OK;
+}
+
+cb::RopeTable table(const cb_plan* p) { return cb::RopeTable{p->rope_tab, p->n_tokens}; }
+
+int32_t k_for_ratio(int32_t r_pct, int32_t n_ctx) {
+  return static_cast<int32_t>((static_cast<int64_t>(r_pct) * n_ctx) / 100);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t cb_version(void) { return 100; }
+
+const char* cb_last_error_string(void) { return g_last_error.c_str(); }
+
+cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
+  CB_TRY(need_ptr(cfg, "cfg"));
+  CB_TRY(need_ptr(out, "out"));
+  *out = nullptr;
+  const cb_config& c = *cfg;
+  if (c.n_chunks < 0 || c.chunk_len <= 0 || c.n_suffix < 0)
+    return fail(CB_ERR_INVALID_ARG, "n_chunks >= 0, chunk_len > 0 and n_suffix >= 0 required");
+  const int64_t n_tokens = (int64_t)c.n_chunks * c.chunk_len + c.n_suffix;
+  if (n_tokens <= 0 || n_tokens > (1 << 24)) return fail(CB_ERR_INVALID_ARG, "n_tokens must be in [1, 2^24]");
+  if (c.hkv <= 0 || c.hq <= 0 || c.hq % c.hkv != 0)
+    return fail(CB_ERR_INVALID_ARG, "hq must be a positive multiple of hkv");
+  const int group = c.hq / c.hkv;
+  if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+    return fail(CB_ERR_UNSUPPORTED, "hq / hkv = %d; supported: 1, 2, 4, 8, 16", group);
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim %d; supported: 64, 128", c.head_dim);
+  if (c.hkv * c.head_dim > 2048) return fail(CB_ERR_UNSUPPORTED, "hkv * head_dim above 2048");
+  if (!(c.rope_theta > 1.0) || !std::isfinite(c.rope_theta)) return fail(CB_ERR_INVALID_ARG, "rope_theta must be > 1");
+  if (c.rope_style != CB_ROPE_HALF && c.rope_style != CB_ROPE_INTERLEAVED)
+    return fail(CB_ERR_INVALID_ARG, "unknown rope_style %d", c.rope_style);
+  if (c.r1_pct < 0 || c.r1_pct > 100 || c.r2_pct < 0 || c.r2_pct > c.r1_pct)
+    return fail(CB_ERR_INVALID_ARG, "need 0 <= r2_pct <= r1_pct <= 100");
+
+  cb_plan* p = new cb_plan();
+  p->cfg = c;
+  p->n_ctx = c.n_chunks * c.chunk_len;
+  p->n_tokens = (int32_t)n_tokens;
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaMalloc(&p->rope_tab, sizeof(float2) * (size_t)n_tokens * (c.head_dim / 2));
+  if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&p->q_pos, sizeof(int32_t) * (size_t)n_tokens);
+  if (e == cudaSuccess) {
+    const int32_t init[2] = {0, -1};
+    e = cudaMemcpy(p->err, init, sizeof(init), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cb::launch_rope_table(p->rope_tab, p->n_tokens, c.head_dim, c.rope_theta, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cb_plan_destroy(p);
+    return cuda_status(e, "cb_plan_create");
+  }
+  *out = p;
+  return CB_OK;
+}
+
+cb_status cb_plan_destroy(cb_plan* plan) {
+  if (plan == nullptr) return CB_OK;
+  cudaDeviceSynchronize();
+  cudaFree(plan->rope_tab);
+  cudaFree(plan->err);
+  cudaFree(plan->q_pos);
+  delete plan;
+  return CB_OK;
+}
+
+cb_status cb_layer_sizes(const cb_plan* plan, int32_t layer, int32_t* n_cand, int32_t* k, int32_t* mq,
+                         int32_t* selects) {
+  CB_TRY(check_plan(plan));
+  if (layer < 1) return fail(CB_ERR_INVALID_ARG, "layer is 1-based, got %d", layer);
+  const int32_t k1 = k_for_ratio(plan->cfg.r1_pct, plan->n_ctx);
+  const int32_t k2 = k_for_ratio(plan->cfg.r2_pct, plan->n_ctx);
+  int32_t c, kk, sel;
+  if (layer == 1) {
+    c = plan->n_ctx, kk = k1, sel = 1;
+  } else if (layer == 2) {
+    c = k1, kk = k2, sel = 1;
+  } else {
+    c = k2, kk = k2, sel = 0;
+  }
+  if (n_cand) *n_cand = c;
+  if (k) *k = kk;
+  if (mq) *mq = kk + plan->cfg.n_suffix;
+  if (selects) *selects = sel;
+  return CB_OK;
+}
+
+cb_status cb_rope_rerotate(cb_plan* plan, void* out, const void* x, const int32_t* in_rows,
+                           const int32_t* out_rows, const int32_t* pos_from, const int32_t* pos_to, int32_t n,
+                           int32_t n_heads, int32_t x_rows, int32_t out_rows_total, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (n < 0 || n_heads <= 0 || x_rows < 0 || out_rows_total < 0)
+    return fail(CB_ERR_INVALID_ARG, "negative size or n_heads <= 0");
+  if (n == 0) return CB_OK;
+  CB_TRY(need_tensor(out, "out"));
+  CB_TRY(need_tensor(x, "x"));
+  CB_TRY(need_ptr(pos_to, "pos_to"));
+  if (out == x && (in_rows != nullptr || out_rows != nullptr))
+    return fail(CB_ERR_INVALID_ARG, "in-place rotation needs in_rows == out_rows == NULL");
+  const cb::RowMap im{in_rows, n, 0, x_rows};
+  const cb::RowMap om{out_rows, n, 0, out_rows_total};
+  return cuda_status(cb::launch_rope_rows(out, x, im, om, pos_from, pos_to, nullptr, n, n_heads,
+                                          plan->cfg.head_dim, plan->cfg.rope_style, table(plan), plan->err,
+                                          static_cast<cudaStream_t>(stream)),
+                     "cb_rope_rerotate");
+}
+
+cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
+                          float* dev, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (m < 0) return fail(CB_ERR_INVALID_ARG, "m < 0");
+  if (m == 0) return CB_OK;
+  if (cand == nullptr && m > plan->n_ctx) return fail(CB_ERR_INVALID_ARG, "m > n_ctx without a candidate list");
+  CB_TRY(need_tensor(v_new, "v_new"));
+  CB_TRY(need_tensor(v_old, "v_old"));
+  CB_TRY(need_ptr(dev, "dev"));
+  return cuda_status(cb::launch_kv_deviation(v_new, v_old, cand, m, plan->n_ctx, plan->cfg.hkv, plan->cfg.head_dim,
+                                             dev, plan->err, static_cast<cudaStream_t>(stream)),
+                     "cb_kv_deviation");
+}
+
+cb_status cb_hkvd_topk(cb_plan* plan, const float* dev, const int32_t* cand, int32_t m, int32_t k,
+                       int32_t* sel_tok, int32_t* sel_row, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (m < 0 || k < 0 || k > m) return fail(CB_ERR_INVALID_ARG, "need 0 <= k <= m (k=%d, m=%d)", k, m);
+  if (k == 0) return CB_OK;
+  CB_TRY(need_ptr(dev, "dev"));
+  CB_TRY(need_ptr(sel_tok, "sel_tok"));
+  CB_TRY(need_ptr(sel_row, "sel_row"));
+  return cuda_status(cb::launch_hkvd_topk(dev, cand, m, k, sel_tok, sel_row, plan->err,
+                                          static_cast<cudaStream_t>(stream)),
+                     "cb_hkvd_topk");
+}
+
+cb_status cb_fuse_scatter(cb_plan* plan, void* k_fused, void* v_fused, const void* k_new, const void* v_new,
+                          const int32_t* sel_tok, int32_t k, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (k < 0 || k > plan->n_ctx) return fail(CB_ERR_INVALID_ARG, "need 0 <= k <= n_ctx");
+  if (k + plan->cfg.n_suffix == 0) return CB_OK;
+  CB_TRY(need_tensor(k_fused, "k_fused"));
+  CB_TRY(need_tensor(v_fused, "v_fused"));
+  CB_TRY(need_tensor(k_new, "k_new"));
+  CB_TRY(need_tensor(v_new, "v_new"));
+  if (k > 0) CB_TRY(need_ptr(sel_tok, "sel_tok"));
+  return cuda_status(cb::launch_fuse_scatter(k_fused, v_fused, k_new, v_new, sel_tok, k, plan->n_ctx,
+                                             plan->n_tokens, plan->cfg.hkv, plan->cfg.head_dim,
+                                             plan->cfg.rope_style, table(plan), plan->err,
+                                             static_cast<cudaStream_t>(stream)),
+                     "cb_fuse_scatter");
+}
+
+cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
+                            const void* v, int32_t n_keys, float scale, void* out, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (mq < 0 || n_keys < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
+  if (mq == 0) return CB_OK;
+  if (n_keys == 0) return fail(CB_ERR_INVALID_ARG, "n_keys == 0 with queries to answer");
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_ptr(q_pos, "q_pos"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  CB_TRY(need_tensor(out, "out"));
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)plan->cfg.head_dim);
+  return cuda_status(cb::launch_hkvd_attention(q, q_pos, mq, k, v, n_keys, plan->cfg.hq, plan->cfg.hkv,
+                                               plan->cfg.head_dim, scale, out, plan->err,
+                                               static_cast<cudaStream_t>(stream)),
+                     "cb_hkvd_attention");
+}
+
+cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
+  CB_TRY(check_plan(plan));
+  CB_TRY(need_ptr(io, "io"));
+  int32_t n_cand, k, mq, selects;
+  CB_TRY(cb_layer_sizes(plan, layer, &n_cand, &k, &mq, &selects));
+  CB_TRY(need_tensor(io->k_old, "io.k_old"));
+  CB_TRY(need_tensor(io->v_old, "io.v_old"));
+  CB_TRY(need_tensor(io->k_new, "io.k_new"));
+  CB_TRY(need_tensor(io->v_new, "io.v_new"));
+  CB_TRY(need_tensor(io->q, "io.q"));
+  CB_TRY(need_tensor(io->k_fused, "io.k_fused"));
+  CB_TRY(need_tensor(io->v_fused, "io.v_fused"));
+  if (mq > 0) {
+    CB_TRY(need_tensor(io->q_rot, "io.q_rot"));
+    CB_TRY(need_tensor(io->out, "io.out"));
+  }
+  if (k > 0) {
+    CB_TRY(need_ptr(io->sel_tok, "io.sel_tok"));
+    CB_TRY(need_ptr(io->sel_row, "io.sel_row"));
+  }
+  if (layer >= 2 && n_cand > 0) CB_TRY(need_ptr(io->cand, "io.cand"));
+  if (selects && n_cand > 0) CB_TRY(need_ptr(io->dev, "io.dev"));
+  const auto& c = plan->cfg;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cb::RopeTable t = table(plan);
+  const int32_t* cand = layer == 1 ? nullptr : io->cand;
+
+  if (selects) {
+    CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, n_cand, plan->n_ctx, c.hkv, c.head_dim,
+                                               io->dev, plan->err, s),
+                       "deviation"));
+    CB_TRY(cuda_status(cb::launch_hkvd_topk(io->dev, cand, n_cand, k, io->sel_tok, io->sel_row, plan->err, s),
+                       "top-k"));
+  } else {
+    CB_TRY(cuda_status(cb::launch_copy_selection(cand, n_cand, io->sel_tok, io->sel_row, s), "selection copy"));
+  }
+  CB_TRY(cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
+                                           io->sel_tok, k, plan->n_ctx, c.chunk_len, plan->n_tokens, c.hkv,
+                                           c.head_dim, c.rope_style, t, plan->err, s),
+                     "fuse"));
+  if (mq == 0) return CB_OK;
+  const cb::RowMap im{io->sel_tok, k, plan->n_ctx, plan->n_tokens};
+  const cb::RowMap om{nullptr, mq, 0, mq};
+  CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, plan->q_pos, mq, c.hq,
+                                          c.head_dim, c.rope_style, t, plan->err, s),
+                     "query encode"));
+  return cuda_status(cb::launch_hkvd_attention(io->q_rot, plan->q_pos, mq, io->k_fused, io->v_fused, plan->n_tokens,
+                                               c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
+                                               io->out, plan->err, s),
+                     "attention");
+}
+
+cb_status cb_check(cb_plan* plan) {
+  CB_TRY(check_plan(plan));
+  int32_t h[2] = {0, -1};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(h, plan->err, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) {
+    const int32_t init[2] = {0, -1};
+    e = cudaMemcpy(plan->err, init, sizeof(init), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) return cuda_status(e, "cb_check");
+  if (h[0] == 0) return CB_OK;
+  const bool timeout = (h[0] & cb::kErrTimeout) != 0;
+  return fail(timeout ? CB_ERR_TIMEOUT : CB_ERR_DEVICE_CHECK,
+              "device check failed: flags 0x%x (1 rope range, 2 index, 4 order, 8 timeout), first at %d", h[0], h[1]);
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Device helpers shared by the blend's kernels (bf16 packing, error word).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cb {
+
+// Bits of the plan's device error word (err[0]); err[1] keeps the first offending index.
+enum DevErr : int32_t {
+  kErrRopeRange = 1,   // |pos_to - pos_from| outside the cos/sin table
+  kErrIndex = 2,       // a token / row id outside its tensor
+  kErrOrder = 4,       // a list that must be strictly ascending is not
+  kErrTimeout = 8,     // a bounded device wait gave up
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int32_t flag, int32_t detail) {
+  if (err == nullptr) return;
+  atomicOr(err, flag);
+  atomicCAS(err + 1, -1, detail);
+}
+
+// 8 bf16 in a uint4 -> 8 floats (exact widening).
+__device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+  f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xffff0000u);
+  f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+
+// Two floats -> packed bf16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// Streaming 16-byte loads/stores: read-once data should not displace L2-resident tables.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, const uint4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+}  // namespace cb

@@ -1,0 +1,62 @@
+// Host-side launchers of the blend's kernels (internal to the library; the
+// public interface is include/cacheblend.h). Every launcher only enqueues on
+// `stream` and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cb {
+
+// Row index map: row i -> (i < k ? (idx ? idx[i] : i) : base + (i - k)); rows at or
+// beyond `limit` (the tensor's row count) are rejected by the kernel.
+struct RowMap {
+  const int32_t* idx;
+  int32_t k;
+  int32_t base;
+  int32_t limit;
+};
+
+struct RopeTable {
+  const float2* tab;  // [len][head_dim / 2] (cos, sin) of p * theta^(-2j/D)
+  int32_t len;
+};
+
+cudaError_t launch_rope_table(float2* tab, int32_t len, int32_t head_dim, double theta, cudaStream_t s);
+
+// out[omap(i)] = R_{pos_to(i) - pos_from(i)} x[imap(i)], i in [0, n).
+// pos_to == nullptr: pos_to(i) = imap(i) (encode at the token's own position).
+// pos_from == nullptr: pos_from(i) = 0. pos_out (optional) receives pos_to(i).
+cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap, const int32_t* pos_from,
+                             const int32_t* pos_to, int32_t* pos_out, int32_t n, int32_t n_heads,
+                             int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_kv_deviation(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
+                                int32_t n_rows, int32_t hkv, int32_t head_dim, float* dev, int32_t* err,
+                                cudaStream_t s);
+
+cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,
+                             int32_t* sel_row, int32_t* err, cudaStream_t s);
+
+// Scatter encoded recomputed rows (sel_tok[0..k) and the suffix) into the fused cache.
+cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new, const void* v_new,
+                                const int32_t* sel_tok, int32_t k, int32_t n_ctx, int32_t n_tokens,
+                                int32_t hkv, int32_t head_dim, int32_t style, RopeTable t, int32_t* err,
+                                cudaStream_t s);
+
+// One pass over all n_tokens rows: cached rows re-rotated by their chunk offset,
+// selected and suffix rows encoded from k_new / v_new.
+cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, const void* v_old,
+                              const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
+                              int32_t n_ctx, int32_t chunk_len, int32_t n_tokens, int32_t hkv,
+                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_copy_selection(const int32_t* cand, int32_t m, int32_t* sel_tok, int32_t* sel_row,
+                                  cudaStream_t s);
+
+// Causal GQA attention over compact RoPE-encoded query rows.
+cudaError_t launch_hkvd_attention(const void* q, const int32_t* q_pos, int32_t mq, const void* k,
+                                  const void* v, int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim,
+                                  float scale, void* out, int32_t* err, cudaStream_t s);
+
+}  // namespace cb

@@ -1,0 +1,538 @@
+// HBM-streaming kernels of the blend: RoPE table, row rotation (re-rotation
+// of cached keys and encoding of recomputed rows), V deviation, fused-cache
+// construction and scatter, and the single-block HKVD top-k.
+//
+// Sources: "数学推导" §RoPE 位置编码的相对位置不变性证明 (pair rotation),
+// §CacheBlend 中的应用 (k_new = R_{p_new - p_old} k_old), §形式化 (fused KV),
+// §近似解 (TopK of ||V_new - V_old||^2); "rag的kvcache问题" §渐进式过滤机制.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cb {
+
+namespace {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ int map_row(const RowMap& m, int i) {
+  return i < m.k ? (m.idx ? m.idx[i] : i) : m.base + (i - m.k);
+}
+
+// ---------------------------------------------------------------------------
+// RoPE cos/sin table: tab[p][j] = (cos a, sin a), a = p * theta^(-2j/D), fp64 then fp32.
+__global__ void rope_table_kernel(float2* tab, int len, int half, int head_dim, double log2_theta) {
+  const long long total = (long long)len * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(idx / half);
+    const int j = (int)(idx % half);
+    const double inv = exp2(-(2.0 * j / head_dim) * log2_theta);
+    double s, c;
+    sincos((double)p * inv, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+// Rotate one row of n_heads x D bf16 by the table row `cs` (sign of sin flipped when neg).
+// One warp per row; 16-byte accesses; src may equal dst.
+template <int STYLE>
+__device__ __forceinline__ void rotate_row(uint8_t* dst, const uint8_t* src, int n_heads, int head_dim,
+                                           const float2* __restrict__ cs, bool neg, int lane) {
+  constexpr int B = 4;
+  if (STYLE == 0) {
+    // pair (j, j + D/2): a unit is 8 consecutive j of one head, lo and hi halves.
+    const int per_head = head_dim / 16;
+    const int units = n_heads * per_head;
+    const int half_bytes = head_dim;  // D/2 elements * 2 bytes
+    for (int u0 = lane; u0 < units; u0 += kWarp * B) {
+      uint4 lo[B], hi[B];
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int u = u0 + kWarp * q;
+        if (u < units) {
+          const int h = u / per_head, c = u % per_head;
+          const uint8_t* p = src + (size_t)h * head_dim * 2 + c * 16;
+          lo[q] = ld_stream(p);
+          hi[q] = ld_stream(p + half_bytes);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int u = u0 + kWarp * q;
+        if (u < units) {
+          const int h = u / per_head, c = u % per_head;
+          float a[8], b[8], oa[8], ob[8];
+          unpack8(lo[q], a);
+          unpack8(hi[q], b);
+          const float4* t4 = reinterpret_cast<const float4*>(cs + c * 8);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 t = __ldg(t4 + e);
+            const float c0 = t.x, s0 = neg ? -t.y : t.y, c1 = t.z, s1 = neg ? -t.w : t.w;
+            oa[2 * e] = a[2 * e] * c0 - b[2 * e] * s0;
+            ob[2 * e] = a[2 * e] * s0 + b[2 * e] * c0;
+            oa[2 * e + 1] = a[2 * e + 1] * c1 - b[2 * e + 1] * s1;
+            ob[2 * e + 1] = a[2 * e + 1] * s1 + b[2 * e + 1] * c1;
+          }
+          uint8_t* p = dst + (size_t)h * head_dim * 2 + c * 16;
+          st_stream(p, pack8(oa));
+          st_stream(p + half_bytes, pack8(ob));
+        }
+      }
+    }
+  } else {
+    // pair (2j, 2j + 1): a unit is one 16-byte vector = 4 pairs.
+    const int per_head = head_dim / 8;
+    const int units = n_heads * per_head;
+    for (int u0 = lane; u0 < units; u0 += kWarp * B) {
+      uint4 v[B];
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int u = u0 + kWarp * q;
+        if (u < units) v[q] = ld_stream(src + (size_t)u * 16);
+      }
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        const int u = u0 + kWarp * q;
+        if (u < units) {
+          const int c = u % per_head;
+          float a[8], o[8];
+          unpack8(v[q], a);
+          const float4* t4 = reinterpret_cast<const float4*>(cs + c * 4);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float4 t = __ldg(t4 + e);
+            const float c0 = t.x, s0 = neg ? -t.y : t.y, c1 = t.z, s1 = neg ? -t.w : t.w;
+            o[4 * e + 0] = a[4 * e + 0] * c0 - a[4 * e + 1] * s0;
+            o[4 * e + 1] = a[4 * e + 0] * s0 + a[4 * e + 1] * c0;
+            o[4 * e + 2] = a[4 * e + 2] * c1 - a[4 * e + 3] * s1;
+            o[4 * e + 3] = a[4 * e + 2] * s1 + a[4 * e + 3] * c1;
+          }
+          st_stream(dst + (size_t)u * 16, pack8(o));
+        }
+      }
+    }
+  }
+}
+
+// Copy one row of `bytes` (multiple of 16) with a warp.
+__device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int bytes, int lane) {
+  constexpr int B = 4;
+  const int vecs = bytes / 16;
+  for (int u0 = lane; u0 < vecs; u0 += kWarp * B) {
+    uint4 v[B];
+#pragma unroll
+    for (int q = 0; q < B; ++q)
+      if (u0 + kWarp * q < vecs) v[q] = ld_stream(src + (size_t)(u0 + kWarp * q) * 16);
+#pragma unroll
+    for (int q = 0; q < B; ++q)
+      if (u0 + kWarp * q < vecs) st_stream(dst + (size_t)(u0 + kWarp * q) * 16, v[q]);
+  }
+}
+
+template <int STYLE>
+__global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint8_t* x, RowMap imap,
+                                                        RowMap omap, const int32_t* pos_from,
+                                                        const int32_t* pos_to, int32_t* pos_out, int n,
+                                                        int n_heads, int head_dim, RopeTable t,
+                                                        int32_t* err) {
+  const int lane = threadIdx.x % kWarp;
+  const int warps = gridDim.x * (blockDim.x / kWarp);
+  const size_t row_bytes = (size_t)n_heads * head_dim * 2;
+  const int half = head_dim / 2;
+  for (int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; i < n; i += warps) {
+    const int src_row = map_row(imap, i);
+    const int dst_row = map_row(omap, i);
+    const int to = pos_to ? pos_to[i] : src_row;
+    const int from = pos_from ? pos_from[i] : 0;
+    const int delta = to - from;
+    const int ad = delta < 0 ? -delta : delta;
+    if (pos_out && lane == 0) pos_out[i] = to;
+    if (src_row < 0 || dst_row < 0 || src_row >= imap.limit || dst_row >= omap.limit) {
+      if (lane == 0) record_error(err, kErrIndex, i);
+      continue;
+    }
+    if (ad >= t.len) {
+      if (lane == 0) record_error(err, kErrRopeRange, i);
+      continue;
+    }
+    rotate_row<STYLE>(out + dst_row * row_bytes, x + src_row * row_bytes, n_heads, head_dim,
+                      t.tab + (size_t)ad * half, delta < 0, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// V deviation, canonical order: lane l sums chunks l, l+32, ... (8 elements each)
+// as acc = fl(acc + fl(d*d)), d = fl(v_new - v_old); then a xor butterfly.
+template <int CPL>  // chunks per lane (ceil(E / 256))
+__global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* v_new, const uint8_t* v_old,
+                                                           const int32_t* cand, int m, int n_rows,
+                                                           int elems, float* dev, int32_t* err) {
+  const int lane = threadIdx.x % kWarp;
+  const int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  if (i >= m) return;
+  const int t = cand ? cand[i] : i;
+  if (t < 0 || t >= n_rows) {
+    if (lane == 0) {
+      dev[i] = __int_as_float(0x7fc00000);
+      record_error(err, kErrIndex, i);
+    }
+    return;
+  }
+  const int chunks = elems / 8;
+  const size_t row_bytes = (size_t)elems * 2;
+  const uint8_t* pn = v_new + (size_t)t * row_bytes;
+  const uint8_t* po = v_old + (size_t)t * row_bytes;
+  uint4 a[CPL], b[CPL];
+#pragma unroll
+  for (int r = 0; r < CPL; ++r) {
+    const int c = lane + kWarp * r;
+    if (c < chunks) {
+      a[r] = ld_stream(pn + (size_t)c * 16);
+      b[r] = ld_stream(po + (size_t)c * 16);
+    }
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int r = 0; r < CPL; ++r) {
+    const int c = lane + kWarp * r;
+    if (c < chunks) {
+      float x[8], y[8];
+      unpack8(a[r], x);
+      unpack8(b[r], y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = __fsub_rn(x[e], y[e]);
+        acc = __fadd_rn(acc, __fmul_rn(d, d));
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+  if (lane == 0) dev[i] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Top-k by MSB-first 8-bit radix select on order-preserving keys, then a
+// stable compaction. One block of 1024 threads.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kTopkThreads = 1024;
+
+__global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __restrict__ dev,
+                                                                  const int32_t* __restrict__ cand, int m,
+                                                                  int k, int32_t* sel_tok, int32_t* sel_row,
+                                                                  int32_t* err) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_remaining;
+  __shared__ int warp_eq[32], warp_sel[32], warp_eq_ex[32], warp_sel_ex[32];
+  __shared__ int s_base_eq, s_base_sel, s_tile_eq, s_tile_sel;
+  const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+  if (tid == 0) {
+    s_prefix = 0;
+    s_mask = 0;
+    s_remaining = k;
+    s_base_eq = 0;
+    s_base_sel = 0;
+  }
+  // candidate ids must be strictly ascending (the output order relies on it)
+  if (cand) {
+    for (int i = tid; i + 1 < m; i += kTopkThreads)
+      if (cand[i] >= cand[i + 1]) record_error(err, kErrOrder, i);
+  }
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int d = tid; d < 256; d += kTopkThreads) hist[d] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    for (int i = tid; i < m; i += kTopkThreads) {
+      const uint32_t key = order_key(dev[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits [248 - 8l, 256 - 8l), scanned from the top digit down
+      uint32_t c[8];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = hist[255 - 8 * lane - e];
+        sum += c[e];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const uint32_t before = incl - sum;
+      const uint32_t need = (uint32_t)s_remaining;
+      if (before < need && need <= incl) {
+        uint32_t cum = before;
+        for (int e = 0; e < 8; ++e) {
+          if (cum + c[e] >= need) {
+            const uint32_t digit = 255u - 8u * lane - e;
+            s_prefix = prefix | (digit << shift);
+            s_mask = mask | (255u << shift);
+            s_remaining = (int)(need - cum);
+            break;
+          }
+          cum += c[e];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t thr = s_prefix;
+  const int need_eq = s_remaining;  // keys equal to thr to keep, lowest rows first
+  const uint32_t below = (1u << lane) - 1u;
+  for (int base = 0; base < m; base += kTopkThreads) {
+    const int i = base + tid;
+    const uint32_t key = i < m ? order_key(dev[i]) : 0u;
+    const bool gt = i < m && key > thr;
+    const bool eq = i < m && key == thr;
+    const uint32_t eq_mask = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) warp_eq[warp] = __popc(eq_mask);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_eq[lane];
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+      }
+      warp_eq_ex[lane] = incl - v;
+      if (lane == 31) s_tile_eq = incl;
+    }
+    __syncthreads();
+    const int eq_rank = s_base_eq + warp_eq_ex[warp] + __popc(eq_mask & below);
+    const bool sel = gt || (eq && eq_rank < need_eq);
+    const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) warp_sel[warp] = __popc(sel_mask);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_sel[lane];
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+      }
+      warp_sel_ex[lane] = incl - v;
+      if (lane == 31) s_tile_sel = incl;
+    }
+    __syncthreads();
+    if (sel) {
+      const int pos = s_base_sel + warp_sel_ex[warp] + __popc(sel_mask & below);
+      if (pos < k) {
+        sel_tok[pos] = cand ? cand[i] : i;
+        sel_row[pos] = i;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      s_base_eq += s_tile_eq;
+      s_base_sel += s_tile_sel;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused cache: rows [r0, r0 + kRowsPerCta) per block, one warp per row.
+constexpr int kFuseRows = 16;
+constexpr int kFuseThreads = 256;
+
+// Mark the members of the ascending list sel[0..k) that fall in [r0, r0 + kFuseRows).
+__device__ __forceinline__ void mark_block(const int32_t* sel, int k, int r0, int n_ctx, uint8_t* is_sel,
+                                           int32_t* err) {
+  __shared__ int s_lo;
+  const int tid = threadIdx.x;
+  if (tid < kFuseRows) is_sel[tid] = 0;
+  if (tid == 0) {
+    int lo = 0, hi = k;  // first index with sel[idx] >= r0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sel[mid] < r0) lo = mid + 1; else hi = mid;
+    }
+    s_lo = lo;
+  }
+  __syncthreads();
+  if (tid < kFuseRows) {
+    const int j = s_lo + tid;
+    if (j < k) {
+      const int t = sel[j];
+      if (t < 0 || t >= n_ctx) record_error(err, kErrIndex, j);
+      else if (j > 0 && sel[j - 1] >= t) record_error(err, kErrOrder, j);
+      else if (t < r0 + kFuseRows) is_sel[t - r0] = 1;
+    }
+  }
+  __syncthreads();
+}
+
+template <int STYLE>
+__global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
+    uint8_t* k_fused, uint8_t* v_fused, const uint8_t* k_old, const uint8_t* v_old, const uint8_t* k_new,
+    const uint8_t* v_new, const int32_t* sel, int k, int n_ctx, int chunk_len, int n_tokens, int hkv,
+    int head_dim, RopeTable t, int32_t* err) {
+  __shared__ uint8_t is_sel[kFuseRows];
+  const int r0 = blockIdx.x * kFuseRows;
+  mark_block(sel, k, r0, n_ctx, is_sel, err);
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  const size_t row_bytes = (size_t)hkv * head_dim * 2;
+  const int half = head_dim / 2;
+  for (int r = warp; r < kFuseRows; r += kFuseThreads / kWarp) {
+    const int tok = r0 + r;
+    if (tok >= n_tokens) break;
+    const bool fresh = tok >= n_ctx || is_sel[r];
+    const int pos = fresh ? tok : (tok / chunk_len) * chunk_len;  // encode at p, or move by the chunk start
+    if (pos >= t.len) {
+      if (lane == 0) record_error(err, kErrRopeRange, tok);
+      continue;
+    }
+    const uint8_t* ks = (fresh ? k_new : k_old) + tok * row_bytes;
+    const uint8_t* vs = (fresh ? v_new : v_old) + tok * row_bytes;
+    rotate_row<STYLE>(k_fused + tok * row_bytes, ks, hkv, head_dim, t.tab + (size_t)pos * half, false, lane);
+    copy_row(v_fused + tok * row_bytes, vs, (int)row_bytes, lane);
+  }
+}
+
+template <int STYLE>
+__global__ void __launch_bounds__(kFuseThreads) fuse_scatter_kernel(uint8_t* k_fused, uint8_t* v_fused,
+                                                                    const uint8_t* k_new, const uint8_t* v_new,
+                                                                    const int32_t* sel, int k, int n_ctx,
+                                                                    int n_tokens, int hkv, int head_dim,
+                                                                    RopeTable t, int32_t* err) {
+  const int lane = threadIdx.x % kWarp;
+  const int warps = gridDim.x * (blockDim.x / kWarp);
+  const int rows = k + (n_tokens - n_ctx);
+  const size_t row_bytes = (size_t)hkv * head_dim * 2;
+  const int half = head_dim / 2;
+  for (int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; i < rows; i += warps) {
+    const int tok = i < k ? sel[i] : n_ctx + (i - k);
+    if (tok < 0 || tok >= n_tokens || (i < k && tok >= n_ctx) || (i > 0 && i < k && sel[i - 1] >= tok)) {
+      if (lane == 0) record_error(err, i < k && i > 0 && tok < n_ctx && tok >= 0 ? kErrOrder : kErrIndex, i);
+      continue;
+    }
+    if (tok >= t.len) {
+      if (lane == 0) record_error(err, kErrRopeRange, tok);
+      continue;
+    }
+    rotate_row<STYLE>(k_fused + tok * row_bytes, k_new + tok * row_bytes, hkv, head_dim,
+                      t.tab + (size_t)tok * half, false, lane);
+    copy_row(v_fused + tok * row_bytes, v_new + tok * row_bytes, (int)row_bytes, lane);
+  }
+}
+
+__global__ void copy_selection_kernel(const int32_t* cand, int m, int32_t* sel_tok, int32_t* sel_row) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < m; i += gridDim.x * blockDim.x) {
+    sel_tok[i] = cand ? cand[i] : i;
+    sel_row[i] = i;
+  }
+}
+
+int grid_for_warps(long long warps_needed, int warps_per_block) {
+  long long b = (warps_needed + warps_per_block - 1) / warps_per_block;
+  if (b < 1) b = 1;
+  if (b > 152LL * 64) b = 152LL * 64;
+  return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(float2* tab, int32_t len, int32_t head_dim, double theta, cudaStream_t s) {
+  const int half = head_dim / 2;
+  const long long total = (long long)len * half;
+  const int blocks = (int)((total + 255) / 256 < 152 * 8 ? (total + 255) / 256 : 152 * 8);
+  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(tab, len, half, head_dim, log2(theta));
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap, const int32_t* pos_from,
+                             const int32_t* pos_to, int32_t* pos_out, int32_t n, int32_t n_heads,
+                             int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int grid = grid_for_warps(n, 8);
+  if (style == 0)
+    rope_rows_kernel<0><<<grid, 256, 0, s>>>((uint8_t*)out, (const uint8_t*)x, imap, omap, pos_from, pos_to,
+                                             pos_out, n, n_heads, head_dim, t, err);
+  else
+    rope_rows_kernel<1><<<grid, 256, 0, s>>>((uint8_t*)out, (const uint8_t*)x, imap, omap, pos_from, pos_to,
+                                             pos_out, n, n_heads, head_dim, t, err);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_kv_deviation(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
+                                int32_t n_rows, int32_t hkv, int32_t head_dim, float* dev, int32_t* err,
+                                cudaStream_t s) {
+  if (m <= 0) return cudaSuccess;
+  const int elems = hkv * head_dim;
+  const int cpl = (elems + 255) / 256;
+  const int grid = (m + 7) / 8;
+  const uint8_t* a = (const uint8_t*)v_new;
+  const uint8_t* b = (const uint8_t*)v_old;
+  if (cpl <= 1) kv_deviation_kernel<1><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
+  else if (cpl <= 2) kv_deviation_kernel<2><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
+  else if (cpl <= 4) kv_deviation_kernel<4><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
+  else if (cpl <= 8) kv_deviation_kernel<8><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
+  else return cudaErrorInvalidValue;
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,
+                             int32_t* sel_row, int32_t* err, cudaStream_t s) {
+  if (k <= 0 || m <= 0) return cudaSuccess;
+  hkvd_topk_kernel<<<1, kTopkThreads, 0, s>>>(dev, cand, m, k, sel_tok, sel_row, err);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new, const void* v_new,
+                                const int32_t* sel_tok, int32_t k, int32_t n_ctx, int32_t n_tokens,
+                                int32_t hkv, int32_t head_dim, int32_t style, RopeTable t, int32_t* err,
+                                cudaStream_t s) {
+  const int rows = k + (n_tokens - n_ctx);
+  if (rows <= 0) return cudaSuccess;
+  const int grid = grid_for_warps(rows, kFuseThreads / kWarp);
+  if (style == 0)
+    fuse_scatter_kernel<0><<<grid, kFuseThreads, 0, s>>>((uint8_t*)k_fused, (uint8_t*)v_fused,
+                                                         (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok,
+                                                         k, n_ctx, n_tokens, hkv, head_dim, t, err);
+  else
+    fuse_scatter_kernel<1><<<grid, kFuseThreads, 0, s>>>((uint8_t*)k_fused, (uint8_t*)v_fused,
+                                                         (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok,
+                                                         k, n_ctx, n_tokens, hkv, head_dim, t, err);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, const void* v_old,
+                              const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
+                              int32_t n_ctx, int32_t chunk_len, int32_t n_tokens, int32_t hkv,
+                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s) {
+  if (n_tokens <= 0) return cudaSuccess;
+  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows;
+  auto* kf = (uint8_t*)k_fused;
+  auto* vf = (uint8_t*)v_fused;
+  if (style == 0)
+    blend_fuse_kernel<0><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
+                                                       (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
+                                                       n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+  else
+    blend_fuse_kernel<1><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
+                                                       (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
+                                                       n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_copy_selection(const int32_t* cand, int32_t m, int32_t* sel_tok, int32_t* sel_row,
+                                  cudaStream_t s) {
+  if (m <= 0) return cudaSuccess;
+  copy_selection_kernel<<<(m + 255) / 256, 256, 0, s>>>(cand, m, sel_tok, sel_row);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace cb

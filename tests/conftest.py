@@ -8,3 +8,35 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def cb():
+    """The built CUDA library's Python binding (GPU tests only)."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    from rag_kv_cache_gb300.build import build
+
+    build()
+    import rag_kv_cache_gb300 as cbm
+
+    return cbm
+
+
+def assert_close_bf16(got, ref, atol=2e-2, rtol=1e-2, what=""):
+    """|got - ref| <= atol + rtol * |ref| elementwise (the blend's bf16 tolerance)."""
+    import numpy as np
+
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    err = np.abs(got - ref)
+    lim = atol + rtol * np.abs(ref)
+    bad = err > lim
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; "
+                           f"max abs err {err.max():.3e}")

@@ -1,0 +1,128 @@
+"""Whole-layer parity: cb_blend_layer against the oracle's blend, on the five workloads.
+
+HKVD sets, candidate rows, deviations and fused V are compared bit for bit;
+fused K, encoded queries and attention outputs within 2e-2 abs + 1e-2 rel.
+At full size the attention is checked on seeded samples of query rows (the
+oracle computes those rows one by one); everything else is checked whole.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_close_bf16
+from oracle.blend import blend_layer, gradual_filter_schedule
+from oracle.deviation import bf16_bits_to_f64
+from workloads import get_config
+from workloads.generator import generate_layer, hkvd_noise_sets
+from workloads.torch_io import bf16_bits, layer_tensors
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu_layers(cb, cfg, layers, style="half", r1=None, r2=None):
+    """Run layers 1..max(layers) on the GPU; return {layer: outputs} for the requested ones."""
+    plan = cb.Plan.from_config(cfg, rope_style=style, r1_pct=r1, r2_pct=r2)
+    sets = hkvd_noise_sets(cfg)
+    bufs = [cb.LayerBuffers(plan), cb.LayerBuffers(plan)]  # ping-pong: S_{l-1} is C_l
+    cand = None
+    results = {}
+    for layer in range(1, max(layers) + 1):
+        inp = generate_layer(cfg, layer, sets)
+        t = layer_tensors(inp)
+        b = bufs[layer % 2]
+        cb.cb_blend_layer(plan, layer, cand=cand, bufs=b, **t)
+        n_cand, k, mq, selects = plan.layer_sizes(layer)
+        plan.check()
+        if layer in layers:
+            results[layer] = dict(
+                inp=inp, k=k, mq=mq, selects=selects,
+                dev=b.dev[:n_cand].cpu().numpy().copy() if selects else None,
+                sel_tok=b.sel_tok[:k].cpu().numpy().copy(), sel_row=b.sel_row[:k].cpu().numpy().copy(),
+                k_fused=bf16_bits(b.k_fused), v_fused=bf16_bits(b.v_fused),
+                q_rot=bf16_bits(b.q_rot[:mq]), out=bf16_bits(b.out[:mq]))
+        cand = b.sel_tok
+    plan.close()
+    return results
+
+
+def oracle_layers(cfg, layers, style="half", attention_rows=None):
+    """The oracle's blend for the requested layers (selection chain followed from layer 1)."""
+    sets = hkvd_noise_sets(cfg)
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
+    cand = np.arange(cfg.n_ctx)
+    out = {}
+    for layer, k, selects in sched[: max(layers)]:
+        inp = generate_layer(cfg, layer, sets)
+        want = layer in layers
+        rows = attention_rows(k + cfg.n_suffix, layer) if (want and attention_rows) else None
+        res = blend_layer(cfg, inp, layer, cand, k, selects, style,
+                          attention_rows=(rows if want else False))
+        if want:
+            out[layer] = res
+        cand = res.sel_tok
+    return out
+
+
+def compare(g, o, cfg, rows=None):
+    assert np.array_equal(g["sel_tok"], o.sel_tok)
+    assert np.array_equal(g["sel_row"], o.sel_row)
+    if o.dev is not None:
+        assert np.array_equal(g["dev"].view(np.uint32), o.dev.view(np.uint32))
+    assert np.array_equal(bf16_bits_to_f64(g["v_fused"]), o.v_fused)
+    assert_close_bf16(bf16_bits_to_f64(g["k_fused"]), o.k_fused, what="fused K")
+    assert_close_bf16(bf16_bits_to_f64(g["q_rot"]), o.q_rot, what="encoded Q")
+    got = bf16_bits_to_f64(g["out"])
+    if rows is None:
+        assert_close_bf16(got, o.out, what="attention")
+    else:
+        assert_close_bf16(got[rows], o.out[rows], what="attention (sampled rows)")
+
+
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+def test_tiny_layer_exact(cb, style):
+    cfg = get_config("tiny")
+    g = run_gpu_layers(cb, cfg, [1], style)[1]
+    o = oracle_layers(cfg, [1], style)[1]
+    compare(g, o, cfg)
+    # the noise model's high-deviation set is what the selection finds
+    assert set(g["sel_tok"].tolist()) == set(g["inp"].hkvd_set.tolist())
+
+
+def test_small_multilayer_gradual_filter(cb):
+    cfg = dataclasses.replace(get_config("mistral7b"), name="small5", config_id=91, n_chunks=5, chunk_len=96,
+                              n_suffix=24, layers=5)
+    g = run_gpu_layers(cb, cfg, [1, 2, 3, 4, 5])
+    o = oracle_layers(cfg, [1, 2, 3, 4, 5])
+    for layer in range(1, 6):
+        compare(g[layer], o[layer], cfg)
+    assert np.array_equal(g[4]["sel_tok"], g[2]["sel_tok"])
+
+
+@pytest.mark.parametrize("r", [5, 10, 15, 30, 50, 100])
+def test_ratio_sweep(cb, r):
+    cfg = get_config("sweep").with_ratio(r)
+    rng = np.random.default_rng(r)
+    pick = lambda mq, layer: np.sort(rng.choice(mq, size=min(mq, 192), replace=False))
+    g = run_gpu_layers(cb, cfg, [1])[1]
+    o = oracle_layers(cfg, [1], attention_rows=pick)[1]
+    compare(g, o, cfg, rows=np.flatnonzero(~np.isnan(o.out[:, 0, 0])))
+    if r == 100:
+        assert g["sel_tok"].tolist() == list(range(cfg.n_ctx))
+
+
+@pytest.mark.parametrize("name,layers", [("mistral7b", [1, 2, 3]), ("llama70b", [1, 2, 3]), ("long32k", [1])])
+def test_full_size_workloads(cb, name, layers):
+    cfg = get_config(name)
+    rng = np.random.default_rng(cfg.config_id)
+    # sampled rows: the first and last query rows, the suffix's first row, and a seeded spread
+    def pick(mq, layer):
+        k = mq - cfg.n_suffix
+        fixed = np.array([0, k - 1, k, mq - 1]) if k > 0 else np.array([0, mq - 1])
+        return np.unique(np.concatenate([fixed, rng.choice(mq, size=min(mq, 60), replace=False)]))
+    g = run_gpu_layers(cb, cfg, layers)
+    o = oracle_layers(cfg, layers, attention_rows=pick)
+    for layer in layers:
+        compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])))

@@ -1,0 +1,262 @@
+"""Per-kernel parity of the CUDA library against the CPU oracle, through the C ABI.
+
+Integer and byte results (deviation bits, selected sets, copied V rows) are
+compared bit for bit; rotated keys and attention outputs within
+2e-2 absolute + 1e-2 relative (bf16 storage, fp32 accumulation).
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_close_bf16
+from oracle.attention import causal_gqa_attention
+from oracle.deviation import bf16_bits_to_f64, deviation_canonical_f32
+from oracle.rope import rerotate, rope_rotate, round_bf16
+from oracle.topk import hkvd_topk
+from workloads import get_config
+from workloads.generator import f32_to_bf16_bits, generate_layer
+from workloads.torch_io import bf16_bits, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).cuda()
+
+
+def _shape(name, **kw):
+    return dataclasses.replace(get_config(name), **kw)
+
+
+def _plan(cb, cfg, style="half", r1=None, r2=None):
+    return cb.Plan.from_config(cfg, rope_style=style, r1_pct=r1, r2_pct=r2)
+
+
+# ---------------------------------------------------------------- rotation
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+@pytest.mark.parametrize("name", ["tiny", "mistral7b", "llama70b"])
+def test_rerotate_cached_keys(cb, name, style):
+    cfg = get_config(name)
+    if name != "tiny":
+        cfg = dataclasses.replace(cfg, n_chunks=3, chunk_len=200, n_suffix=40)
+    plan = _plan(cb, cfg, style)
+    inp = generate_layer(cfg, 1)
+    n_ctx = cfg.n_ctx
+    p_old = np.arange(n_ctx) % cfg.chunk_len
+    p_new = np.arange(n_ctx)
+    x = bf16_tensor(inp.k_old)
+    out = torch.zeros_like(x)
+    cb.cb_rope_rerotate(plan, out, x, _i32(p_new), pos_from=_i32(p_old))
+    plan.check()
+    ref = round_bf16(rerotate(bf16_bits_to_f64(inp.k_old), p_old, p_new, cfg.rope_theta, style))
+    got = bf16_bits_to_f64(bf16_bits(out))
+    assert_close_bf16(got, ref, what="re-rotated keys")
+    assert np.mean(got == ref) > 0.99  # fp32 math vs fp64: at most rare 1-ulp differences
+    # chunk 0 has delta 0: the bytes are copied unchanged
+    assert np.array_equal(bf16_bits(out)[: cfg.chunk_len], inp.k_old[: cfg.chunk_len])
+
+
+def test_encode_in_place_and_negative_delta(cb):
+    cfg = get_config("tiny")
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(11)
+    bits = f32_to_bf16_bits(rng.standard_normal((300, 4, 64)).astype(np.float32))
+    pos = rng.integers(0, cfg.n_tokens, size=300)
+    x = bf16_tensor(bits)
+    cb.cb_rope_rerotate(plan, x, x, _i32(pos))  # in place, encode at pos
+    ref = round_bf16(rope_rotate(bf16_bits_to_f64(bits), pos, cfg.rope_theta))
+    assert_close_bf16(bf16_bits_to_f64(bf16_bits(x)), ref, what="encode in place")
+    # rotating back by -pos recovers the input within bf16 rounding
+    back = torch.empty_like(x)
+    cb.cb_rope_rerotate(plan, back, x, _i32(np.zeros(300)), pos_from=_i32(pos))
+    plan.check()
+    assert_close_bf16(bf16_bits_to_f64(bf16_bits(back)), bf16_bits_to_f64(bits), what="inverse rotation")
+
+
+def test_gather_scatter_rows_and_range_check(cb):
+    cfg = get_config("tiny")
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(12)
+    src = f32_to_bf16_bits(rng.standard_normal((50, 2, 64)).astype(np.float32))
+    x = bf16_tensor(src)
+    out = torch.zeros(80, 2, 64, dtype=torch.bfloat16, device="cuda")
+    in_rows = rng.choice(50, 20, replace=False)
+    out_rows = rng.choice(80, 20, replace=False)
+    pos = rng.integers(0, 500, 20)
+    cb.cb_rope_rerotate(plan, out, x, _i32(pos), in_rows=_i32(in_rows), out_rows=_i32(out_rows))
+    plan.check()
+    got = bf16_bits_to_f64(bf16_bits(out))
+    ref = round_bf16(rope_rotate(bf16_bits_to_f64(src[in_rows]), pos, cfg.rope_theta))
+    assert_close_bf16(got[out_rows], ref, what="gathered rows")
+    untouched = np.setdiff1d(np.arange(80), out_rows)
+    assert np.all(got[untouched] == 0)
+    # a delta beyond the table and a row beyond the tensor are skipped and reported
+    bad_pos = pos.copy()
+    bad_pos[3] = cfg.n_tokens + 5
+    bad_in = in_rows.copy()
+    bad_in[7] = 50
+    before = bf16_bits(out).copy()
+    cb.cb_rope_rerotate(plan, out, x, _i32(bad_pos), in_rows=_i32(bad_in), out_rows=_i32(out_rows))
+    with pytest.raises(cb.CacheBlendError) as e:
+        plan.check()
+    assert e.value.status == 5
+    after = bf16_bits(out)
+    assert np.array_equal(after[out_rows[3]], before[out_rows[3]])
+    assert np.array_equal(after[out_rows[7]], before[out_rows[7]])
+    plan.check()  # the error word was cleared
+
+
+# ---------------------------------------------------------------- deviation
+@pytest.mark.parametrize("hkv,d", [(2, 64), (8, 128), (16, 128), (1, 64), (3, 64)])
+def test_deviation_bit_exact(cb, hkv, d):
+    cfg = dataclasses.replace(get_config("tiny"), hkv=hkv, hq=hkv * 2, head_dim=d, n_chunks=4, chunk_len=333)
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(hkv * 100 + d)
+    n_ctx = cfg.n_ctx
+    v_old = f32_to_bf16_bits(rng.standard_normal((n_ctx, hkv, d)).astype(np.float32))
+    scale = np.exp(rng.uniform(-9, 1, size=(n_ctx, 1, 1))).astype(np.float32)
+    v_new = np.concatenate([
+        f32_to_bf16_bits((v_old.astype(np.uint32) << 16).view(np.float32)
+                         + scale * rng.standard_normal((n_ctx, hkv, d)).astype(np.float32)),
+        f32_to_bf16_bits(rng.standard_normal((cfg.n_suffix, hkv, d)).astype(np.float32))])
+    v_new[5] = v_old[5]  # an exact-zero deviation
+    cand = np.sort(rng.choice(n_ctx, size=n_ctx // 3, replace=False))
+    dev = torch.empty(cand.size, dtype=torch.float32, device="cuda")
+    cb.cb_kv_deviation(plan, bf16_tensor(v_new), bf16_tensor(v_old), _i32(cand), cand.size, dev)
+    ref = deviation_canonical_f32(v_new[cand], v_old[cand])
+    assert np.array_equal(dev.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # identity candidate list
+    dev_all = torch.empty(n_ctx, dtype=torch.float32, device="cuda")
+    cb.cb_kv_deviation(plan, bf16_tensor(v_new), bf16_tensor(v_old), None, n_ctx, dev_all)
+    plan.check()
+    ref_all = deviation_canonical_f32(v_new[:n_ctx], v_old)
+    assert np.array_equal(dev_all.cpu().numpy().view(np.uint32), ref_all.view(np.uint32))
+    assert dev_all[5].item() == 0.0
+
+
+def test_deviation_golden_rounding_cases(cb):
+    # the hand-derived cases that pin the summation order, run on the GPU
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "deviation_rounding.txt")
+    cfg = dataclasses.replace(get_config("tiny"), hkv=4, hq=8, head_dim=128)
+    plan = _plan(cb, cfg)
+    for line in open(path, encoding="utf-8"):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, e, entries, expect = (s.strip() for s in line.split("|"))
+        vn = np.zeros(512, np.float32)
+        vo = np.zeros(512, np.float32)
+        for ent in entries.split():
+            i, a, b = ent.split(":")
+            vn[int(i)] = float.fromhex(a) if "x" in a else float(a)
+            vo[int(i)] = float.fromhex(b) if "x" in b else float(b)
+        dev = torch.empty(1, dtype=torch.float32, device="cuda")
+        cb.cb_kv_deviation(plan, bf16_tensor(f32_to_bf16_bits(vn).reshape(1, 4, 128)),
+                           bf16_tensor(f32_to_bf16_bits(vo).reshape(1, 4, 128)), None, 1, dev)
+        assert dev.item() == float.fromhex(expect), name
+
+
+# ---------------------------------------------------------------- top-k
+@pytest.mark.parametrize("m", [1, 7, 64, 1000, 1024, 1025, 3072, 32768, 40000])
+def test_topk_bit_exact_with_ties(cb, m):
+    plan = _plan(cb, get_config("tiny"))
+    rng = np.random.default_rng(m)
+    cand = np.sort(rng.choice(max(2 * m, 10), size=m, replace=False))
+    pools = [rng.choice(np.array([0.0, 0.5, 1.0, 3.0], np.float32), size=m),
+             rng.standard_normal(m).astype(np.float32) ** 2,
+             np.zeros(m, np.float32)]
+    for dev in pools:
+        for k in sorted({1, m // 7, m // 2, m - 1, m} - {0}):
+            d = torch.as_tensor(dev).cuda()
+            st = torch.full((k,), -1, dtype=torch.int32, device="cuda")
+            sr = torch.full((k,), -1, dtype=torch.int32, device="cuda")
+            cb.cb_hkvd_topk(plan, d, _i32(cand), m, k, st, sr)
+            rt, rr = hkvd_topk(dev, cand, k)
+            assert np.array_equal(st.cpu().numpy(), rt) and np.array_equal(sr.cpu().numpy(), rr), (m, k)
+    plan.check()
+
+
+def test_topk_lognormal_near_ties(cb):
+    # the ratio-sweep noise model: bf16 rounding makes many deviations exactly equal
+    cfg = get_config("sweep")
+    inp = generate_layer(cfg, 1)
+    plan = _plan(cb, cfg, r1=100, r2=100)
+    n = cfg.n_ctx
+    dev = torch.empty(n, dtype=torch.float32, device="cuda")
+    cb.cb_kv_deviation(plan, bf16_tensor(inp.v_new), bf16_tensor(inp.v_old), None, n, dev)
+    ref_dev = deviation_canonical_f32(inp.v_new[:n], inp.v_old)
+    assert np.array_equal(dev.cpu().numpy().view(np.uint32), ref_dev.view(np.uint32))
+    assert np.unique(ref_dev).size < n  # ties are present
+    for r in cfg.sweep_pct:
+        k = r * n // 100
+        st = torch.empty(k, dtype=torch.int32, device="cuda")
+        sr = torch.empty(k, dtype=torch.int32, device="cuda")
+        cb.cb_hkvd_topk(plan, dev, None, n, k, st, sr)
+        rt, _ = hkvd_topk(ref_dev, np.arange(n), k)
+        assert np.array_equal(st.cpu().numpy(), rt), r
+    plan.check()
+
+
+# ---------------------------------------------------------------- fuse / scatter
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+def test_fuse_scatter(cb, style):
+    cfg = get_config("tiny")
+    plan = _plan(cb, cfg, style)
+    inp = generate_layer(cfg, 1)
+    rng = np.random.default_rng(5)
+    sel = np.sort(rng.choice(cfg.n_ctx, 76, replace=False))
+    kf = bf16_tensor(np.zeros((cfg.n_tokens, 2, 64), np.uint16))
+    vf = bf16_tensor(np.zeros((cfg.n_tokens, 2, 64), np.uint16))
+    cb.cb_fuse_scatter(plan, kf, vf, bf16_tensor(inp.k_new), bf16_tensor(inp.v_new), _i32(sel), sel.size)
+    plan.check()
+    rows = np.concatenate([sel, np.arange(cfg.n_ctx, cfg.n_tokens)])
+    others = np.setdiff1d(np.arange(cfg.n_tokens), rows)
+    kb, vb = bf16_bits(kf), bf16_bits(vf)
+    assert np.array_equal(vb[rows], inp.v_new[rows]) and np.all(vb[others] == 0) and np.all(kb[others] == 0)
+    ref = round_bf16(rope_rotate(bf16_bits_to_f64(inp.k_new[rows]), rows, cfg.rope_theta, style))
+    assert_close_bf16(bf16_bits_to_f64(kb[rows]), ref, what="scattered keys")
+
+
+# ---------------------------------------------------------------- attention
+def _attention_case(cb, hq, hkv, d, n_keys, q_pos, seed, scale_q=1.0):
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=max(n_keys - 1, 1), n_suffix=1)
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(seed)
+    mq = len(q_pos)
+    q = f32_to_bf16_bits((scale_q * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    return bf16_bits_to_f64(bf16_bits(out)), ref
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (32, 8, 128), (64, 8, 128), (8, 8, 128), (16, 1, 64)])
+def test_attention_sparse_queries(cb, hq, hkv, d):
+    rng = np.random.default_rng(hq + d)
+    n_keys = 1000
+    q_pos = np.sort(rng.choice(n_keys, size=150, replace=False))
+    got, ref = _attention_case(cb, hq, hkv, d, n_keys, q_pos, seed=hq * 7 + d)
+    assert_close_bf16(got, ref, what=f"attention hq={hq} hkv={hkv} d={d}")
+
+
+@pytest.mark.parametrize("n_keys", [1, 2, 127, 128, 129, 300, 2049])
+def test_attention_all_positions(cb, n_keys):
+    # every position queried: the full-recompute case (r = 100%)
+    q_pos = np.arange(n_keys)
+    got, ref = _attention_case(cb, 32, 8, 128, n_keys, q_pos, seed=n_keys)
+    assert_close_bf16(got, ref, what=f"attention n_keys={n_keys}")
+
+
+def test_attention_peaked_scores_force_rescale(cb):
+    # large query norms make the running max jump between key tiles (O rescaling path)
+    rng = np.random.default_rng(3)
+    q_pos = np.sort(rng.choice(1500, size=100, replace=False))
+    got, ref = _attention_case(cb, 8, 2, 64, 1500, q_pos, seed=9, scale_q=6.0)
+    assert_close_bf16(got, ref, what="peaked attention")
