@@ -180,6 +180,15 @@ typedef struct cb_layer_io {
  *   the query rows encoded, and the attention. */
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream);
 
+/* cb_blend_layer with timing marks: events[0..5] are cudaEvent_t handles (any
+ * may be NULL) recorded on `stream` before the deviation, before the top-k,
+ * before the fused-cache pass, before the query encoding, before the
+ * attention and after it (stages a layer skips leave two adjacent marks).
+ * Under stream capture they become external event-record nodes. */
+#define CB_N_STAGE_EVENTS 6
+cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                               void* const* events);
+
 /* Synchronise the plan's device, read and clear its error word. Returns
  * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
  * cb_last_error_string). Off the hot path. */

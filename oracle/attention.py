@@ -16,10 +16,14 @@ from __future__ import annotations
 import numpy as np
 
 
-def causal_gqa_attention(q, q_pos, k, v, scale: float | None = None, block: int = 256):
+def causal_gqa_attention(q, q_pos, k, v, scale: float | None = None, block: int = 256,
+                         return_vscale: bool = False):
     """O[i, h] = sum_{j <= q_pos[i]} softmax_j(q[i,h] . k[j,g] * scale) v[j,g], g = h // G.
 
     q [mq, Hq, D], q_pos [mq]; k, v [N, Hkv, D] with key j at position j.
+    With return_vscale, also returns sum_j softmax_j |v[j,g]| per output element:
+    the magnitude that rounding the softmax weights multiplies (an error scale
+    for comparisons, not part of the attention).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -33,6 +37,7 @@ def causal_gqa_attention(q, q_pos, k, v, scale: float | None = None, block: int 
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     out = np.zeros((mq, hq, d), dtype=np.float64)
+    vscale = np.zeros((mq, hq, d), dtype=np.float64) if return_vscale else None
     for b0 in range(0, mq, block):
         b1 = min(mq, b0 + block)
         pos = q_pos[b0:b1]
@@ -47,4 +52,6 @@ def causal_gqa_attention(q, q_pos, k, v, scale: float | None = None, block: int 
             p = np.exp(s)
             p = p / p.sum(axis=1, keepdims=True)
             out[b0:b1, h, :] = p @ v[:kend, g, :]
-    return out
+            if return_vscale:
+                vscale[b0:b1, h, :] = p @ np.abs(v[:kend, g, :])
+    return (out, vscale) if return_vscale else out

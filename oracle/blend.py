@@ -61,6 +61,7 @@ class LayerResult:
     q_tok: np.ndarray           # query tokens: S_l then the suffix
     q_rot: np.ndarray           # fp64 holding bf16 values [mq, Hq, D]
     out: np.ndarray | None      # fp64 [mq, Hq, D] (rows not requested are NaN)
+    out_vscale: np.ndarray | None = None  # sum_j softmax_j |v_j| per output element (error scale)
 
 
 def blend_layer(cfg, inp, layer: int, cand, k: int, selects: bool, style: str = "half",
@@ -91,14 +92,15 @@ def blend_layer(cfg, inp, layer: int, cand, k: int, selects: bool, style: str = 
 
     q_tok = rows_new
     q_rot = round_bf16(rope_rotate(bf16_bits_to_f64(inp.q[q_tok]), q_tok, cfg.rope_theta, style))
-    out = None
+    out = vs = None
     if attention_rows is None:
-        out = causal_gqa_attention(q_rot, q_tok, k_f, v_f)
+        out, vs = causal_gqa_attention(q_rot, q_tok, k_f, v_f, return_vscale=True)
     elif attention_rows is not False:
         rows = np.asarray(attention_rows, dtype=np.int64)
         out = np.full(q_rot.shape, np.nan)
-        out[rows] = causal_gqa_attention(q_rot[rows], q_tok[rows], k_f, v_f)
-    return LayerResult(layer, cand, k, dev, sel_tok, sel_row, k_f, v_f, is_new, q_tok, q_rot, out)
+        vs = np.full(q_rot.shape, np.nan)
+        out[rows], vs[rows] = causal_gqa_attention(q_rot[rows], q_tok[rows], k_f, v_f, return_vscale=True)
+    return LayerResult(layer, cand, k, dev, sel_tok, sel_row, k_f, v_f, is_new, q_tok, q_rot, out, vs)
 
 
 def blend_request(cfg, layer_inputs, style: str = "half", attention_rows=None):

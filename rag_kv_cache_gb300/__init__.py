@@ -148,8 +148,14 @@ class LayerBuffers:
         self.out = torch.empty(max(mq1, 1), plan.hq, plan.head_dim, **bf)
 
 
-def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None):
-    """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer))."""
+def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None,
+                   events=None):
+    """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer)).
+
+    events: optional sequence of 6 torch.cuda.Event (or None) recorded at the stage
+    boundaries (cb_blend_layer_timed); each event must have been recorded once before
+    so that its CUDA handle exists.
+    """
     io = _lib.CbLayerIO(
         _ptr(k_old, torch.bfloat16, "k_old"), _ptr(v_old, torch.bfloat16, "v_old"),
         _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
@@ -157,4 +163,8 @@ def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: La
         _ptr(bufs.sel_tok, torch.int32, "sel_tok"), _ptr(bufs.sel_row, torch.int32, "sel_row"),
         _ptr(bufs.k_fused, torch.bfloat16, "k_fused"), _ptr(bufs.v_fused, torch.bfloat16, "v_fused"),
         _ptr(bufs.q_rot, torch.bfloat16, "q_rot"), _ptr(bufs.out, torch.bfloat16, "out"))
-    check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))
+    if events is None:
+        check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))
+        return
+    arr = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else None) for e in events])
+    check(_lib.load().cb_blend_layer_timed(plan.handle, layer, ctypes.byref(io), _stream(stream), arr))

@@ -235,7 +235,30 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                      "cb_hkvd_attention");
 }
 
+static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                                  void* const* events);
+
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
+  return blend_layer_impl(plan, layer, io, stream, nullptr);
+}
+
+cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                               void* const* events) {
+  return blend_layer_impl(plan, layer, io, stream, events);
+}
+
+static cb_status record_mark(void* const* events, int i, cudaStream_t s) {
+  if (events == nullptr || events[i] == nullptr) return CB_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e == cudaSuccess)
+    e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
+                                 cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+  return cuda_status(e, "stage event");
+}
+
+static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                                  void* const* events) {
   CB_TRY(check_plan(plan));
   CB_TRY(need_ptr(io, "io"));
   int32_t n_cand, k, mq, selects;
@@ -262,29 +285,39 @@ cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, vo
   const cb::RopeTable t = table(plan);
   const int32_t* cand = layer == 1 ? nullptr : io->cand;
 
+  CB_TRY(record_mark(events, 0, s));
   if (selects) {
     CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, n_cand, plan->n_ctx, c.hkv, c.head_dim,
                                                io->dev, plan->err, s),
                        "deviation"));
+    CB_TRY(record_mark(events, 1, s));
     CB_TRY(cuda_status(cb::launch_hkvd_topk(io->dev, cand, n_cand, k, io->sel_tok, io->sel_row, plan->err, s),
                        "top-k"));
   } else {
+    CB_TRY(record_mark(events, 1, s));
     CB_TRY(cuda_status(cb::launch_copy_selection(cand, n_cand, io->sel_tok, io->sel_row, s), "selection copy"));
   }
+  CB_TRY(record_mark(events, 2, s));
   CB_TRY(cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
                                            io->sel_tok, k, plan->n_ctx, c.chunk_len, plan->n_tokens, c.hkv,
                                            c.head_dim, c.rope_style, t, plan->err, s),
                      "fuse"));
-  if (mq == 0) return CB_OK;
+  CB_TRY(record_mark(events, 3, s));
+  if (mq == 0) {
+    CB_TRY(record_mark(events, 4, s));
+    return record_mark(events, 5, s);
+  }
   const cb::RowMap im{io->sel_tok, k, plan->n_ctx, plan->n_tokens};
   const cb::RowMap om{nullptr, mq, 0, mq};
   CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, plan->q_pos, mq, c.hq,
                                           c.head_dim, c.rope_style, t, plan->err, s),
                      "query encode"));
-  return cuda_status(cb::launch_hkvd_attention(io->q_rot, plan->q_pos, mq, io->k_fused, io->v_fused, plan->n_tokens,
+  CB_TRY(record_mark(events, 4, s));
+  CB_TRY(cuda_status(cb::launch_hkvd_attention(io->q_rot, plan->q_pos, mq, io->k_fused, io->v_fused, plan->n_tokens,
                                                c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
                                                io->out, plan->err, s),
-                     "attention");
+                     "attention"));
+  return record_mark(events, 5, s);
 }
 
 cb_status cb_check(cb_plan* plan) {

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import assert_close_bf16
+from conftest import assert_close_attention, assert_close_bf16
 from oracle.blend import blend_layer, gradual_filter_schedule
 from oracle.deviation import bf16_bits_to_f64
 from workloads import get_config
@@ -76,9 +76,9 @@ def compare(g, o, cfg, rows=None):
     assert_close_bf16(bf16_bits_to_f64(g["q_rot"]), o.q_rot, what="encoded Q")
     got = bf16_bits_to_f64(g["out"])
     if rows is None:
-        assert_close_bf16(got, o.out, what="attention")
+        assert_close_attention(got, o.out, o.out_vscale)
     else:
-        assert_close_bf16(got[rows], o.out[rows], what="attention (sampled rows)")
+        assert_close_attention(got[rows], o.out[rows], o.out_vscale[rows], what="attention (sampled rows)")
 
 
 @pytest.mark.parametrize("style", ["half", "interleaved"])

@@ -180,7 +180,8 @@ def test_topk_bit_exact_with_ties(cb, m):
 
 
 def test_topk_lognormal_near_ties(cb):
-    # the ratio-sweep noise model: bf16 rounding makes many deviations exactly equal
+    # the ratio-sweep noise model: per-token scales spread over decades, so the
+    # selection boundary falls among closely spaced deviations
     cfg = get_config("sweep")
     inp = generate_layer(cfg, 1)
     plan = _plan(cb, cfg, r1=100, r2=100)
@@ -189,7 +190,6 @@ def test_topk_lognormal_near_ties(cb):
     cb.cb_kv_deviation(plan, bf16_tensor(inp.v_new), bf16_tensor(inp.v_old), None, n, dev)
     ref_dev = deviation_canonical_f32(inp.v_new[:n], inp.v_old)
     assert np.array_equal(dev.cpu().numpy().view(np.uint32), ref_dev.view(np.uint32))
-    assert np.unique(ref_dev).size < n  # ties are present
     for r in cfg.sweep_pct:
         k = r * n // 100
         st = torch.empty(k, dtype=torch.int32, device="cuda")
