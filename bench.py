@@ -1,0 +1,482 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 CacheBlend per-layer KV blend.
+
+Metric: context tokens blended per second per layer = n_ctx * layers / step
+time, where one step is the whole hot path (deviation, top-k under the
+gradual filter, fused cache, query encoding, causal GQA attention) over every
+layer of one synthetic request. Default workload: the Mistral-7B-shaped
+32-layer blend (6 x 512 cached tokens + 64 suffix tokens, 32 q / 8 kv heads,
+head_dim 128, r1 = 30% -> r2 = 15%).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Our arm: inputs resident in HBM (per-layer buffers, 1.6 GB per step, larger
+than L2), each step one CUDA-graph replay of all layers' launches through the
+C ABI; per-stage CUDA events inside the timed graph give each kernel's time.
+`e2e` repeats the metric through the C ABI from pinned host buffers with the
+host-to-device copies of every layer's inputs and the device-to-host copy of
+its outputs inside the timed region. `cpu_baseline` times the CPU oracle on a
+bounded sample (layers 1, 2, 3; per-step time extrapolated as t1 + t2 + 30 t3).
+The reference arm (--impl reference) times the CPU oracle itself, one whole
+layer per step cycling through the layers.
+Under torchrun each rank runs an independent replica (the blend of one
+request does not shard); value = all ranks' tokens / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "context tokens blended/s per layer"
+UNIT = "tokens/s"
+STAGES = ("deviation", "topk", "fuse", "query_encode", "attention")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mistral7b")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(cfg):
+    return (f"{cfg.name}: {cfg.n_chunks}x{cfg.chunk_len} cached + {cfg.n_suffix} suffix tokens, "
+            f"{cfg.hq} q / {cfg.hkv} kv heads, head_dim {cfg.head_dim}, RoPE theta {cfg.rope_theta:g}, "
+            f"{cfg.layers} layers, r1 {cfg.r1_pct}% -> r2 {cfg.r2_pct}%")
+
+
+def data_desc(cfg):
+    noise = (f"sigma {cfg.sigma_hi} on a seeded {cfg.hkvd_frac:.0%} set, {cfg.sigma_lo} elsewhere, "
+             f"{cfg.swap_frac:.0%} of the set swapped per layer" if cfg.noise == "set"
+             else f"lognormal per-token scale (mu {cfg.lognormal_mu}, sigma {cfg.lognormal_sigma})")
+    return f"synthetic: seeded N(0,1) bf16 caches and queries; recomputed K/V = cached + noise ({noise})"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("clocks.sm", "clocks.max.sm", "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[3:7]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- oracle (CPU)
+def oracle_chain(cfg, inputs):
+    """Candidate lists of every layer (the oracle's own selection chain)."""
+    from oracle.blend import gradual_filter_schedule
+    from oracle.deviation import deviation_canonical_f32
+    from oracle.topk import hkvd_topk
+
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
+    cand = np.arange(cfg.n_ctx)
+    chain = []
+    for (layer, k, selects), inp in zip(sched, inputs):
+        chain.append((layer, cand, k, selects))
+        if selects:
+            dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
+            cand, _ = hkvd_topk(dev, cand, k)
+    return chain
+
+
+def time_oracle_layer(cfg, inp, layer, cand, k, selects):
+    from oracle.blend import blend_layer
+
+    t0 = time.perf_counter()
+    blend_layer(cfg, inp, layer, cand, k, selects)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, inputs):
+    chain = oracle_chain(cfg, inputs[:3])
+    times = [time_oracle_layer(cfg, inputs[i], *chain[i]) for i in range(min(3, cfg.layers))]
+    if cfg.layers >= 3:
+        t_step = times[0] + times[1] + (cfg.layers - 2) * times[2]
+        sample = (f"oracle on layers 1, 2, 3 of {cfg.name} (all query rows); per-step time extrapolated as "
+                  f"t1 + t2 + {cfg.layers - 2} * t3 = {t_step:.2f} s")
+    else:
+        t_step = sum(times)
+        sample = f"oracle on all {cfg.layers} layer(s) of {cfg.name}"
+    return {"value": cfg.n_ctx * cfg.layers / t_step, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": sample + "; numpy fp64 with its BLAS on all host cores"}
+
+
+def run_reference(args, cfg):
+    from workloads.generator import generate_layer, hkvd_noise_sets
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    sets = hkvd_noise_sets(cfg)
+    inputs = [generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1)]
+    chain = oracle_chain(cfg, inputs)
+    for i in range(args.warmup):
+        time_oracle_layer(cfg, inputs[i % cfg.layers], *chain[i % cfg.layers])
+    total = 0.0
+    for i in range(args.steps):
+        j = (args.warmup + i) % cfg.layers
+        total += time_oracle_layer(cfg, inputs[j], *chain[j])
+    value = cfg.n_ctx * args.steps / total
+    sample = f"each step one whole layer of {cfg.name} by the CPU oracle, cycling through its {cfg.layers} layers"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": data_desc(cfg), "config": {"workload": workload_desc(cfg), "n_ctx": cfg.n_ctx},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+def attention_flops(cfg, sel_tok):
+    q_pos = np.concatenate([np.asarray(sel_tok, dtype=np.int64), np.arange(cfg.n_ctx, cfg.n_tokens)])
+    return 4.0 * cfg.hq * cfg.head_dim * float(np.sum(q_pos + 1))
+
+
+def stage_bytes(cfg, n_cand, k, mq, selects):
+    row_kv = cfg.hkv * cfg.head_dim * 2
+    row_q = cfg.hq * cfg.head_dim * 2
+    return {"deviation": 2.0 * n_cand * row_kv if selects else 0.0,
+            "topk": 8.0 * n_cand if selects else 8.0 * n_cand,
+            "fuse": 4.0 * cfg.n_tokens * row_kv,
+            "query_encode": 2.0 * mq * row_q}
+
+
+def traffic_for(kernel_src):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "rag_kv_cache_gb300", "csrc", kernel_src), "rb").read()
+        entry = rec.get(kernel_src)
+        if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return entry
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import rag_kv_cache_gb300 as cb
+    from rag_kv_cache_gb300.build import build
+    from workloads.generator import generate_layer, hkvd_noise_sets
+    from workloads.torch_io import layer_tensors
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+
+    sets = hkvd_noise_sets(cfg)
+    host_inputs = [generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1)]
+    d_in = [layer_tensors(inp, dev) for inp in host_inputs]
+    plan = cb.Plan.from_config(cfg)
+    bufs = [cb.LayerBuffers(plan, dev) for _ in range(cfg.layers)]
+    sizes = [plan.layer_sizes(layer) for layer in range(1, cfg.layers + 1)]
+    launches_per_step = sum((5 if s[3] else 4) if s[2] > 0 else 3 for s in sizes)
+    stream = torch.cuda.Stream(dev)
+
+    def step(events=None):
+        cand = None
+        for li in range(cfg.layers):
+            cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=bufs[li], stream=stream,
+                              events=None if events is None else events[li], **d_in[li])
+            cand = bufs[li].sel_tok
+
+    # warm up eagerly (first launches configure the kernels), check the device error word
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    stream.synchronize()
+    plan.check()
+
+    n_events = 6
+    use_graph = not args.no_graph
+    chunk = 32
+    ev_sets = [[[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(cfg.layers)]
+               for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for s in ev_sets:  # create the CUDA events
+            for layer_ev in s:
+                for e in layer_ev:
+                    e.record(stream)
+    stream.synchronize()
+
+    graphs = []
+    if use_graph:
+        try:
+            warm = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(warm, stream=stream):
+                step()
+            for s0 in range(0, args.steps, chunk):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for s in range(s0, min(args.steps, s0 + chunk)):
+                        step(ev_sets[s])
+                graphs.append(g)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    warm.replay()
+            stream.synchronize()
+        except Exception as e:  # capture unsupported: fall back to eager launches
+            print(f"bench: CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            use_graph, graphs = False, []
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    with ClockSampler(gpu_index) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            if use_graph:
+                for g in graphs:
+                    g.replay()
+            else:
+                for s in range(args.steps):
+                    step(ev_sets[s])
+            stop.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    plan.check()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = cfg.n_ctx * cfg.layers * args.steps * world / (elapsed_ms / 1e3)
+
+    # per-stage kernel times from the events inside the timed region
+    stage_ms = {s: 0.0 for s in STAGES}
+    attn_ms_by_layer = np.zeros(cfg.layers)
+    for s in range(args.steps):
+        for li in range(cfg.layers):
+            ev = ev_sets[s][li]
+            for i, name in enumerate(STAGES):
+                dt = ev[i].elapsed_time(ev[i + 1])
+                stage_ms[name] += dt
+                if name == "attention":
+                    attn_ms_by_layer[li] += dt
+    flops = np.array([attention_flops(cfg, bufs[li].sel_tok[: sizes[li][1]].cpu().numpy())
+                      for li in range(cfg.layers)])
+    peaks = load_peaks()
+    attn_s = stage_ms["attention"] / 1e3
+    achieved_tf = float(flops.sum()) * args.steps / attn_s / 1e12
+    peak_tf = peaks["bf16_tflops_sustained"]
+    traffic = traffic_for("attention.cu")
+    roofline = {"kernel": "hkvd_attention", "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
+                "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+                "flops_per_step": float(flops.sum()), "launches_per_step": cfg.layers,
+                "avg_launch_us": 1e3 * stage_ms["attention"] / (args.steps * cfg.layers)}
+    stages = {}
+    for name in STAGES:
+        per_step_ms = stage_ms[name] / args.steps
+        entry = {"ms_per_step": per_step_ms}
+        if name in ("deviation", "fuse", "query_encode"):
+            b = sum(stage_bytes(cfg, *sizes[li])[name] for li in range(cfg.layers))
+            if b > 0 and per_step_ms > 0:
+                gbs = b / (per_step_ms / 1e3) / 1e9
+                entry.update({"bytes_per_step": b, "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
+        stages[name] = entry
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": data_desc(cfg),
+            "config": {"workload": workload_desc(cfg), "n_ctx": cfg.n_ctx, "n_tokens": cfg.n_tokens,
+                       "layers": cfg.layers,
+                       "l2": f"inputs larger than L2: {sum(sum(t.numel() * 2 for t in d.values()) for d in d_in) / 1e9:.2f} GB per step",
+                       "cuda_graph": use_graph, "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "stages": stages, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary()}
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, host_inputs[:3])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
+    """Metric through the C ABI with host buffers: H2D of every layer's inputs and D2H of its outputs timed."""
+    import torch
+    import torch.distributed as dist
+
+    from workloads.torch_io import layer_tensors
+
+    h_in = [layer_tensors(inp, "cpu", pin=True) for inp in host_inputs]
+    d_in = [{k: torch.empty_like(v, device=dev) for k, v in h.items()} for h in h_in]
+    h_out = [torch.empty((s[2], cfg.hq, cfg.head_dim), dtype=torch.bfloat16, pin_memory=True) for s in sizes]
+    h_sel = [torch.empty((max(s[1], 1),), dtype=torch.int32, pin_memory=True) for s in sizes]
+    comp = torch.cuda.Stream(dev)
+    h2d = torch.cuda.Stream(dev)
+    d2h = torch.cuda.Stream(dev)
+    layer_done = [torch.cuda.Event() for _ in range(cfg.layers)]
+    copied = [torch.cuda.Event() for _ in range(cfg.layers)]
+    drained = [torch.cuda.Event() for _ in range(cfg.layers)]
+    for e in layer_done + drained:
+        e.record(comp)
+    h2d_bytes = sum(sum(t.numel() * 2 for t in h.values()) for h in h_in)
+    d2h_bytes = sum(o.numel() * 2 + (s[1] * 4) for o, s in zip(h_out, sizes))
+
+    def step():
+        for li in range(cfg.layers):
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(layer_done[li])  # the previous step's layer li has consumed these buffers
+                for k, t in h_in[li].items():
+                    d_in[li][k].copy_(t, non_blocking=True)
+                copied[li].record(h2d)
+        cand = None
+        for li in range(cfg.layers):
+            comp.wait_event(copied[li])
+            comp.wait_event(drained[li])
+            cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=bufs[li], stream=comp, **d_in[li])
+            layer_done[li].record(comp)
+            cand = bufs[li].sel_tok
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(layer_done[li])
+                h_out[li].copy_(bufs[li].out[: sizes[li][2]], non_blocking=True)
+                if sizes[li][1] > 0:
+                    h_sel[li][: sizes[li][1]].copy_(bufs[li].sel_tok[: sizes[li][1]], non_blocking=True)
+                drained[li].record(d2h)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(comp)
+    for _ in range(args.e2e_steps):
+        step()
+    comp.wait_stream(d2h)
+    comp.wait_stream(h2d)
+    stop.record(comp)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    plan.check()
+    return {"value": cfg.n_ctx * cfg.layers * args.e2e_steps * world / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
+            "ms_per_step": ms / args.e2e_steps, "steps": args.e2e_steps}
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        print("bench: --warmup below 3 raised to 3", file=sys.stderr)
+        args.warmup = 3
+    from workloads import get_config
+
+    cfg = get_config(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
