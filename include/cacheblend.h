@@ -189,6 +189,33 @@ cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, vo
 cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
                                void* const* events);
 
+/* HKVD selection that allocates nothing (the pages have no counterpart: this
+ * is a deployment aid). For callers that cannot allocate device memory where
+ * they select tokens, e.g. a serving engine whose own pool owns all free HBM
+ * (a cudaMalloc there fails or fragments the pool), or a latency-critical
+ * path that cannot pay cudaMalloc's implicit device synchronisation; such a
+ * caller cannot create a cb_plan either. Computes exactly what
+ * cb_kv_deviation followed by cb_hkvd_topk compute (same kernels, same
+ * fixed-order fp32 deviation, same tie rule), without a plan:
+ *   v_new, v_old  [>= n_rows, hkv, head_dim] bf16, token-indexed, 16-B aligned
+ *   cand          [m] strictly ascending token ids < n_rows, or NULL (= 0..m-1)
+ *   sel_tok/row   [k] outputs, as cb_hkvd_topk.
+ * The per-candidate deviations live in one array compiled into the library,
+ * CB_NOALLOC_MAX_CANDIDATES floats (256 KiB) on every GPU that loads it,
+ * held until the process exits; m above that limit returns
+ * CB_ERR_INVALID_ARG. The first call on a device looks up that array's device
+ * address (once per device, with the device current), so make the first call
+ * on each device before any stream capture. All calls share the array: calls
+ * whose work overlaps on the GPU (different streams, no ordering between
+ * them) race and can return wrong selections; order them on one stream.
+ * Device-side argument findings are not recorded (there is no plan to hold an
+ * error word): an out-of-range candidate gets a NaN deviation, which ranks
+ * first. Calls no cudaMalloc, cudaFree or allocating library routine. */
+#define CB_NOALLOC_MAX_CANDIDATES 65536
+cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
+                                 int32_t k, int32_t n_rows, int32_t hkv, int32_t head_dim,
+                                 int32_t* sel_tok, int32_t* sel_row, void* stream);
+
 /* Synchronise the plan's device, read and clear its error word. Returns
  * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
  * cb_last_error_string). Off the hot path. */

@@ -132,6 +132,17 @@ def cb_hkvd_attention(plan, q, q_pos, mq, k, v, n_keys, out, scale=0.0, stream=N
         _ptr(out, torch.bfloat16, "out"), _stream(stream)))
 
 
+def cb_hkvd_select_noalloc(v_new, v_old, cand, m, k, n_rows, sel_tok, sel_row, stream=None):
+    """HKVD selection with no allocation anywhere (see cacheblend.h): the deviations
+    between its two kernels live in a fixed array inside the library, so this call
+    needs no plan. For callers that must not allocate device memory where they
+    select tokens. m is at most 65536; calls that overlap on the GPU race."""
+    check(_lib.load().cb_hkvd_select_noalloc(
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(v_old, torch.bfloat16, "v_old"),
+        _ptr(cand, torch.int32, "cand"), m, k, n_rows, v_new.shape[1], v_new.shape[2],
+        _ptr(sel_tok, torch.int32, "sel_tok"), _ptr(sel_row, torch.int32, "sel_row"), _stream(stream)))
+
+
 class LayerBuffers:
     """Device buffers of one layer's outputs, sized for the plan's largest layer."""
 

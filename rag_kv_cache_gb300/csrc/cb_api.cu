@@ -72,6 +72,10 @@ int32_t k_for_ratio(int32_t r_pct, int32_t n_ctx) {
 
 }  // namespace
 
+namespace cb {
+cb_status set_last_error(cb_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace cb
+
 extern "C" {
 
 int32_t cb_version(void) { return 100; }
