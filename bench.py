@@ -262,7 +262,8 @@ def run_ours(args, cfg):
     plan = cb.Plan.from_config(cfg)
     bufs = [cb.LayerBuffers(plan, dev) for _ in range(cfg.layers)]
     sizes = [plan.layer_sizes(layer) for layer in range(1, cfg.layers + 1)]
-    launches_per_step = sum((5 if s[3] else 4) if s[2] > 0 else 3 for s in sizes)
+    # our kernels per layer: deviation + top-k (selecting layers), fuse, query encoding, attention
+    launches_per_step = sum((2 if s[3] else 0) + (3 if s[2] > 0 else 1) for s in sizes)
     stream = torch.cuda.Stream(dev)
 
     def step(events=None):
@@ -362,7 +363,8 @@ def run_ours(args, cfg):
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                 "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
                 "flops_per_step": float(flops.sum()), "launches_per_step": cfg.layers,
-                "avg_launch_us": 1e3 * stage_ms["attention"] / (args.steps * cfg.layers)}
+                "avg_launch_us": 1e3 * stage_ms["attention"] / (args.steps * cfg.layers),
+                "us_by_layer": [round(1e3 * x / args.steps, 2) for x in attn_ms_by_layer]}
     stages = {}
     for name in STAGES:
         per_step_ms = stage_ms[name] / args.steps

@@ -11,13 +11,21 @@
 // so every K/V tile it loads serves all G heads. Key tiles are 128 keys; the
 // CTA visits key tiles 0 .. (largest query position in the tile) / 128.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax + epilogue: thread r owns query row r (TMEM lane r)
-//   warp 4     TMA producer: Q once, then K/V tiles into a 2-stage ring
-//   warp 5     MMA issuer:   S_j = Q K_j^T into TMEM (2 buffers), O += P_j V_j
-// TMEM columns: S buffer 0 [0,128), S buffer 1 [128,256), O [256, 256 + D).
-// P (bf16) overwrites the first 64 columns of its S buffer and is the A
-// operand of the PV MMA straight from TMEM.
+// Roles (352 threads):
+//   WG0, WG1 (warps 0-7) softmax: thread r of each owns query row r (TMEM lane
+//              r); WG0 takes the even key tiles, WG1 the odd ones, each with its
+//              own running max / sum and its own O accumulator, so the two
+//              softmaxes overlap each other and the tensor core; the two partial
+//              results are merged in the epilogue.
+//   warp 8     TMA producer of Q (once) and of K tiles (3-stage ring; a stage
+//              is refilled as soon as its S = Q K^T is done);
+//   warp 9     MMA issuer (tcgen05.mma, bf16 in, fp32 accumulate);
+//   warp 10    TMA producer of V tiles (2-stage ring, refilled after P V).
+// TMEM columns: S buffers [0,128) and [128,256) (tile j uses buffer j % 2),
+// O accumulators [256, 256+D) and [256+D, 256+2D). P (bf16) overwrites the first
+// 64 columns of its S buffer and is the A operand of the PV MMA from TMEM.
+// A softmax thread reads its S row from TMEM in 32-column chunks, the next
+// chunk's load in flight while the current one is processed.
 //
 // Every mbarrier wait is bounded (2 s by the global timer). A wait that gives
 // up records a timeout in the error word, raises a CTA-wide abort flag that
@@ -35,21 +43,26 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kWarpProducer = 4;
-constexpr int kWarpMma = 5;
+constexpr int kKStages = 3;  // depth of the K ring
+constexpr int kVStages = 2;  // depth of the V ring (Q + 3 K + 2 V tiles = 192 KiB for D = 128)
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 128;  // per softmax warpgroup
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpProducerV = 10;
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int s) { return s ? 128u : 0u; }
-constexpr uint32_t kColO = 256;
+__host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int b, int d) { return 256u + (uint32_t)(b * d); }
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kOverflowGuard = 64.0f;    // log2 units: largest exponent the one-pass softmax accepts
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2];
-  uint64_t v_full[2];
-  uint64_t kv_empty[2];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -104,10 +117,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete; false on abort or timeout.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                       int site, bool honour_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: spin with a time limit.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                            int site, bool honour_abort) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -120,6 +132,13 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+
+// Wait for the phase of parity `parity` to complete; false on abort or timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          int site, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, site, honour_abort);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
@@ -207,11 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_maxpos;
+  __shared__ float s_ml[2][2][kBM];  // [warpgroup][max, sum][row]
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base;
-  const uint32_t sK[2] = {base + kQBytes, base + kQBytes + kKVBytes};
-  const uint32_t sV[2] = {base + kQBytes + 2 * kKVBytes, base + kQBytes + 3 * kKVBytes};
+  const uint32_t sK0 = base + kQBytes;
+  const uint32_t sV0 = sK0 + kKStages * kKVBytes;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int lin = blockIdx.x;
@@ -222,13 +242,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars.q_full), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&bars.v_full[s]), 1);
-      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
-      mbar_init(smem_u32(&bars.s_full[s]), 1);
-      mbar_init(smem_u32(&bars.p_full[s]), kSoftmaxThreads);
-      mbar_init(smem_u32(&bars.pv_done[s]), 1);
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars.s_full[b]), 1);
+      mbar_init(smem_u32(&bars.p_full[b]), kSoftmaxThreads / 32);  // one arrival per softmax warp
+      mbar_init(smem_u32(&bars.pv_done[b]), 1);
     }
     mbar_init(smem_u32(&bars.drain), 1);
     s_abort = 0;
@@ -244,88 +269,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // Each softmax thread's query position; padded rows repeat the tile's last token.
+  // Query position of each softmax thread's row; padded rows repeat the tile's last token.
   int my_pos = 0;
-  if (threadIdx.x < kSoftmaxThreads) {
-    const int r = threadIdx.x;
+  if (threadIdx.x < 2 * kSoftmaxThreads) {
+    const int r = threadIdx.x % kBM;
     const int t = min(t0 + r / p.group, t_last);
     int pos = p.q_pos[t];
     if (pos < 0 || pos >= p.n_keys) {
-      record_error(p.err, kErrIndex, t);
+      if (threadIdx.x < kSoftmaxThreads) record_error(p.err, kErrIndex, t);
       pos = pos < 0 ? 0 : p.n_keys - 1;
     }
-    if (r % p.group == 0 && t == t0 + r / p.group && t > 0 && p.q_pos[t - 1] >= p.q_pos[t])
-      record_error(p.err, kErrOrder, t);
+    if (threadIdx.x < kSoftmaxThreads) {
+      if (r % p.group == 0 && t == t0 + r / p.group && t > 0 && p.q_pos[t - 1] >= p.q_pos[t])
+        record_error(p.err, kErrOrder, t);
+      atomicMax(&s_maxpos, pos);
+    }
     my_pos = pos;
-    atomicMax(&s_maxpos, pos);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int n_kv = s_maxpos / kBN + 1;
+  const int n_kv = s_maxpos / kBN + 1;  // key tiles the query tile sees
   volatile int* abort_flag = &s_abort;
 
-  if (warp == kWarpProducer) {
-    if (lane == 0) {
+  if (warp >= 2 * (kSoftmaxThreads / 32)) {
+    if (warp == kWarpProducer && lane == 0) {
       const uint32_t qb = smem_u32(&bars.q_full);
       mbar_expect_tx(qb, kQBytes);
 #pragma unroll
       for (int b = 0; b < kBoxes; ++b) tma_load_4d(sQ + b * kQBox, &tm_q, qb, b * 64, 0, g, t0);
-      int issued = 0;
+      int nk = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(smem_u32(&bars.kv_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.err, 1)) break;
-        const uint32_t kb = smem_u32(&bars.k_full[s]), vb = smem_u32(&bars.v_full[s]);
+        const int sk = j % kKStages;
+        if (j >= kKStages &&
+            !mbar_wait(smem_u32(&bars.k_empty[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1))
+          break;
+        const uint32_t kb = smem_u32(&bars.k_full[sk]);
         mbar_expect_tx(kb, kKVBytes);
 #pragma unroll
-        for (int b = 0; b < kBoxes; ++b) tma_load_3d(sK[s] + b * kKVBox, &tm_k, kb, b * 64, g, j * kBN);
-        mbar_expect_tx(vb, kKVBytes);
-#pragma unroll
-        for (int b = 0; b < kBoxes; ++b) tma_load_3d(sV[s] + b * kKVBox, &tm_v, vb, b * 64, g, j * kBN);
-        issued = j + 1;
+        for (int b = 0; b < kBoxes; ++b)
+          tma_load_3d(sK0 + sk * kKVBytes + b * kKVBox, &tm_k, kb, b * 64, g, j * kBN);
+        nk = j + 1;
       }
       // Before the CTA can exit, every copy issued must have landed.
-      mbar_wait(qb, 0, abort_flag, p.err, 2, false);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
-        mbar_wait(smem_u32(&bars.k_full[j & 1]), (j >> 1) & 1, abort_flag, p.err, 3, false);
-        mbar_wait(smem_u32(&bars.v_full[j & 1]), (j >> 1) & 1, abort_flag, p.err, 4, false);
+      mbar_wait(qb, 0, abort_flag, p.err, 3, false);
+      for (int j = nk - kKStages < 0 ? 0 : nk - kKStages; j < nk; ++j)
+        mbar_wait(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 4, false);
+    } else if (warp == kWarpProducerV && lane == 0) {
+      int nv = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int sv = j % kVStages;
+        if (j >= kVStages &&
+            !mbar_wait(smem_u32(&bars.v_empty[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2))
+          break;
+        const uint32_t vb = smem_u32(&bars.v_full[sv]);
+        mbar_expect_tx(vb, kKVBytes);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b)
+          tma_load_3d(sV0 + sv * kKVBytes + b * kKVBox, &tm_v, vb, b * 64, g, j * kBN);
+        nv = j + 1;
       }
-    }
-    __syncwarp();
-  } else if (warp == kWarpMma) {
-    if (lane == 0) {
+      for (int j = nv - kVStages < 0 ? 0 : nv - kVStages; j < nv; ++j)
+        mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
+    } else if (warp == kWarpMma && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t idesc_o = idesc_bf16(kBM, D, true);
       bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, p.err, 10);
       auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait(smem_u32(&bars.k_full[s]), (j >> 1) & 1, abort_flag, p.err, 11)) return false;
+        const int st = j % kKStages, b = j & 1;
+        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / kKStages) & 1, abort_flag, p.err, 11)) return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int b = ks / 4, kk = ks % 4;
-          const uint64_t a = sdesc(sQ + b * kQBox + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc(sK[s] + b * kKVBox + kk * 32, 16, 1024);
-          mma_ss(tmem + col_s(s), a, bd, idesc_s, ks > 0 ? 1u : 0u);
+          const int bx = ks / 4, kk = ks % 4;
+          const uint64_t a = sdesc(sQ + bx * kQBox + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc(sK0 + st * kKVBytes + bx * kKVBox + kk * 32, 16, 1024);
+          mma_ss(tmem + col_s(b), a, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bars.s_full[s]));
+        tc_commit(smem_u32(&bars.k_empty[st]));
+        tc_commit(smem_u32(&bars.s_full[b]));
         return true;
       };
       if (ok) ok = issue_s(0);
+      if (ok && n_kv > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j & 1;
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(smem_u32(&bars.p_full[s]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
-        if (!mbar_wait(smem_u32(&bars.v_full[s]), (j >> 1) & 1, abort_flag, p.err, 13)) break;
+        const int b = j & 1, st = j % kVStages;
+        if (!mbar_wait(smem_u32(&bars.p_full[b]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
+        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / kVStages) & 1, abort_flag, p.err, 13)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = sdesc(sV[s] + ks * 16 * 128, kKVBox, 1024);
-          mma_ts(tmem + kColO, tmem + col_s(s) + ks * 8, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t bd = sdesc(sV0 + st * kKVBytes + ks * 16 * 128, kKVBox, 1024);
+          mma_ts(tmem + col_o(b, D), tmem + col_s(b) + ks * 8, bd, idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bars.kv_empty[s]));
-        tc_commit(smem_u32(&bars.pv_done[s]));
+        tc_commit(smem_u32(&bars.v_empty[st]));
+        tc_commit(smem_u32(&bars.pv_done[b]));
+        if (j + 2 < n_kv && !issue_s(j + 2)) break;
       }
       // All tensor-core work issued by this CTA completes before TMEM is freed.
       tc_commit(smem_u32(&bars.drain));
@@ -333,97 +373,232 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int r = threadIdx.x;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_ref = -INFINITY, l = 0.0f;
+    const int wg = warp / 4;  // 0: even key tiles, 1: odd key tiles
+    const int r = threadIdx.x % kBM;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    const uint32_t sbar = smem_u32(&bars.s_full[wg]);
+    const uint32_t pbar = smem_u32(&bars.p_full[wg]);
+    const uint32_t obar = smem_u32(&bars.pv_done[wg]);
+    // m_ref: reference max (log2 units) that this warpgroup's O and l are scaled to;
+    // m_seen: the largest row max seen so far (m_ref catches up lazily).
+    float m_ref = -INFINITY, m_seen = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j & 1;
-      const bool w = mbar_wait(smem_u32(&bars.s_full[s]), (j >> 1) & 1, abort_flag, p.err, 20);
+    int it = 0;
+    for (int j = wg; j < n_kv; j += 2, ++it) {
+      const bool w = mbar_wait(sbar, it & 1, abort_flag, p.err, 20 + wg);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t raw[128];
-      tmem_ld_x128(lane_base + col_s(s), raw);
-      float x[128];
-      const int kb = j * kBN;
-      const bool need_mask = kb + kBN - 1 > my_pos;
-      float mx = -INFINITY;
+      const int lim = my_pos - j * kBN;  // columns c <= lim are visible to this row
+      const bool masking = __any_sync(0xffffffffu, lim < kBN - 1);
+      const uint32_t s_addr = lane_base + col_s(wg);
+
+      // Rescale O and l to a new reference (O holds this warpgroup's sum through its previous
+      // tile; that PV is complete because S_j was issued after it).
+      auto rescale_to = [&](float m_new, bool want) -> bool {
+        const bool w2 = mbar_wait(obar, (it - 1) & 1, abort_flag, p.err, 22 + wg);
+        if (!__all_sync(0xffffffffu, w2)) return false;
+        tc_fence_after();
+        const float alpha = want ? ex2(m_ref - m_new) : 1.0f;
+        if (want) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(lane_base + col_o(wg, D) + c0, o);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = __uint_as_float(raw[c]) * p.scale_log2;
-        if (need_mask && kb + c > my_pos) v = -INFINITY;
-        x[c] = v;
-        mx = fmaxf(mx, v);
-      }
-      if (j == 0) {
-        m_ref = mx;
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x32(lane_base + col_o(wg, D) + c0, o);
+        }
+        tmem_st_wait();
+        return true;
+      };
+
+      if (it == 0) {
+        // First tile of this warpgroup: take the row max as the reference (a max-only pass).
+        float pm[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
+        {
+          uint32_t ca[32], cb[32];
+          tmem_ld_x32_async(s_addr, ca);
+          tmem_wait_ld(ca);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
+            uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
+            if (ch < 3) tmem_ld_x32_async(s_addr + (ch + 1) * 32, nxt);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(cur[c]);
+              pm[c & 7] = fmaxf(pm[c & 7], v);
+            }
+            if (ch < 3) tmem_wait_ld(nxt);
+          }
+        }
+        m_ref = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                      fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
       } else {
-        const bool want = mx > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, want)) {
-          // O holds the sum through tile j-1: wait for that PV, then rescale rows that need it.
-          const bool w2 = mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag, p.err, 21);
-          if (!__all_sync(0xffffffffu, w2)) {
+        // Lazy rescale: move the reference up only once the max has grown by more than 2^8.
+        const bool want = m_seen > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, want) && !rescale_to(m_seen, want)) {
+          ok = false;
+          break;
+        }
+      }
+      {
+        // One pass against the current reference. Each 32-key chunk is checked before its
+        // exponentials: every exponent at most kOverflowGuard keeps P and the fp32 sums finite.
+        // P chunk ch (keys 32ch..) is stored in columns 16ch..16ch+15, which hold keys already read.
+        float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;  // reference 0 while nothing was visible
+        float pm[8], ps[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pm[q] = -INFINITY, ps[q] = 0.0f;
+        int bail = 4;  // first chunk that failed the guard
+        {
+          uint32_t ca[32], cb[32];
+          tmem_ld_x32_async(s_addr, ca);
+          tmem_wait_ld(ca);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
+            uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
+            if (ch < 3) tmem_ld_x32_async(s_addr + (ch + 1) * 32, nxt);
+            if (bail == 4) {  // warp-uniform
+              float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(cur[c]);
+                cm[c & 3] = fmaxf(cm[c & 3], v);
+              }
+              const float cmax = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
+              if (__any_sync(0xffffffffu, cmax * p.scale_log2 + neg_m > kOverflowGuard)) {
+                bail = ch;
+              } else {
+                pm[ch] = cmax;
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const float v0 = (masking && ch * 32 + 2 * e > lim) ? -INFINITY : __uint_as_float(cur[2 * e]);
+                  const float v1 =
+                      (masking && ch * 32 + 2 * e + 1 > lim) ? -INFINITY : __uint_as_float(cur[2 * e + 1]);
+                  const float p0 = ex2(fmaf(v0, p.scale_log2, neg_m));
+                  const float p1 = ex2(fmaf(v1, p.scale_log2, neg_m));
+                  ps[e & 7] += p0 + p1;
+                  pk[e] = pack2(p0, p1);
+                }
+                tmem_st_x16(s_addr + ch * 16, pk);
+              }
+            }
+            if (ch < 3) tmem_wait_ld(nxt);
+          }
+        }
+        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * p.scale_log2;
+        if (bail < 4) {
+          // Rare: a row's max jumped past the guard at chunk `bail`. Chunks bail.. are intact in
+          // TMEM; find the tile's max, move O, l, the partial sums and the P chunks already
+          // stored to it, then finish the tile against it.
+          float rm = -INFINITY;
+#pragma unroll 1
+          for (int ch = bail; ch < 4; ++ch) {
+            uint32_t c32[32];
+            tmem_ld_x32(s_addr + ch * 32, c32);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(c32[c]);
+              rm = fmaxf(rm, v);
+            }
+          }
+          mx = fmaxf(mx, rm * p.scale_log2);
+          // The reference never moves down; rows with nothing visible yet keep all-zero values.
+          const float m_eff = -neg_m;  // reference of this tile's P chunks and sums so far
+          const float m_new = fmaxf(m_ref, mx);
+          const float beta = m_new == -INFINITY ? 1.0f : ex2(fminf(m_eff - m_new, 126.0f));
+          if (!rescale_to(m_new, m_new > m_ref)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const float alpha = want ? ex2(m_ref - mx) : 1.0f;
-          if (want) {
-            l *= alpha;
-            m_ref = mx;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ps[q] *= beta;
+#pragma unroll 1
+          for (int ch = 0; ch < bail; ++ch) {
+            uint32_t q16[16];
+            tmem_ld_x16(s_addr + ch * 16, q16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              q16[e] = pack2(__uint_as_float(q16[e] << 16) * beta, __uint_as_float(q16[e] & 0xffff0000u) * beta);
+            tmem_st_x16(s_addr + ch * 16, q16);
           }
+          neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
+#pragma unroll 1
+          for (int ch = bail; ch < 4; ++ch) {
+            uint32_t c32[32];
+            tmem_ld_x32(s_addr + ch * 32, c32);
+            uint32_t pk[16];
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(lane_base + kColO + c0, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_x32(lane_base + kColO + c0, o);
+            for (int e = 0; e < 16; ++e) {
+              const float v0 = (masking && ch * 32 + 2 * e > lim) ? -INFINITY : __uint_as_float(c32[2 * e]);
+              const float v1 = (masking && ch * 32 + 2 * e + 1 > lim) ? -INFINITY : __uint_as_float(c32[2 * e + 1]);
+              const float p0 = ex2(fmaf(v0, p.scale_log2, neg_m));
+              const float p1 = ex2(fmaf(v1, p.scale_log2, neg_m));
+              ps[e & 7] += p0 + p1;
+              pk[e] = pack2(p0, p1);
+            }
+            tmem_st_x16(s_addr + ch * 16, pk);
           }
-          tmem_st_wait();
+        } else if (m_ref == -INFINITY && mx > -INFINITY) {
+          m_ref = 0.0f;  // this pass used reference 0
         }
-      }
-      float sum = 0.0f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2(x[h * 64 + 2 * e] - m_ref);
-          const float p1 = ex2(x[h * 64 + 2 * e + 1] - m_ref);
-          sum += p0 + p1;
-          pk[e] = pack2(p0, p1);
-        }
-        tmem_st_x32(lane_base + col_s(s) + h * 32, pk);
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        m_seen = fmaxf(m_seen, mx);
       }
       tmem_st_wait();
-      l += sum;
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[s]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pbar);
     }
-    if (ok) {
-      const bool w = mbar_wait(smem_u32(&bars.pv_done[(n_kv - 1) & 1]), ((n_kv - 1) >> 1) & 1, abort_flag, p.err, 22);
-      if (__all_sync(0xffffffffu, w)) {
-        tc_fence_after();
-        const int t = t0 + r / p.group;
-        const bool valid = t <= t_last;
-        const float inv = 1.0f / l;
-        uint8_t* dst = p.out + ((size_t)t * p.hq + (size_t)g * p.group + (r % p.group)) * D * 2;
+    const int n_mine = (n_kv - wg + 1) / 2;
+    if (ok && n_mine > 0) {
+      const bool w = mbar_wait(obar, (n_mine - 1) & 1, abort_flag, p.err, 24 + wg);
+      ok = __all_sync(0xffffffffu, w);
+    }
+    // Merge the two warpgroups' partial results; each writes half of the columns.
+    s_ml[wg][0][r] = m_ref;
+    s_ml[wg][1][r] = l;
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
+    ok = ok && !*abort_flag;
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const float m0 = s_ml[0][0][r], m1 = s_ml[1][0][r];
+      const float mm = fmaxf(m0, m1);
+      const float a0 = m0 == -INFINITY ? 0.0f : ex2(m0 - mm);
+      const float a1 = m1 == -INFINITY ? 0.0f : ex2(m1 - mm);
+      const float inv = 1.0f / (s_ml[0][1][r] * a0 + s_ml[1][1][r] * a1);
+      const bool have1 = n_kv > 1;
+      const int t = t0 + r / p.group;
+      const bool valid = t <= t_last;
+      uint8_t* dst = p.out + ((size_t)t * p.hq + (size_t)g * p.group + (r % p.group)) * D * 2;
+#pragma unroll 1
+      for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+        uint32_t o0[32], o1[32];
+        tmem_ld_x32(lane_base + col_o(0, D) + c0, o0);
+        if (have1) tmem_ld_x32(lane_base + col_o(1, D) + c0, o1);
+        if (valid) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(lane_base + kColO + c0, o);
-          if (valid) {
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[q * 8 + e]) * inv;
-              *reinterpret_cast<uint4*>(dst + (c0 + q * 8) * 2) = pack8(f);
+            for (int e = 0; e < 8; ++e) {
+              const float v0 = __uint_as_float(o0[q * 8 + e]) * a0;
+              const float v1 = have1 ? __uint_as_float(o1[q * 8 + e]) * a1 : 0.0f;
+              f[e] = (v0 + v1) * inv;
             }
+            *reinterpret_cast<uint4*>(dst + (c0 + q * 8) * 2) = pack8(f);
           }
         }
       }
@@ -490,7 +665,7 @@ cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = static_cast<uint8_t*>(out);
   p.err = err;
-  size_t smem = 1024 + (size_t)(kBM + 4 * kBN) * D * 2;
+  size_t smem = 1024 + (size_t)(kBM + (kKStages + kVStages) * kBN) * D * 2;
   if (smem < 117 * 1024) smem = 117 * 1024;  // one CTA per SM: the CTA takes all 512 TMEM columns
   static bool configured = false;
   if (!configured) {

@@ -112,6 +112,7 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
   if (e == cudaSuccess) e = cudaMalloc(&p->rope_tab, sizeof(float2) * (size_t)n_tokens * (c.head_dim / 2));
   if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&p->q_pos, sizeof(int32_t) * (size_t)n_tokens);
+
   if (e == cudaSuccess) {
     const int32_t init[2] = {0, -1};
     e = cudaMemcpy(p->err, init, sizeof(init), cudaMemcpyHostToDevice);
@@ -290,6 +291,7 @@ static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_i
   const int32_t* cand = layer == 1 ? nullptr : io->cand;
 
   CB_TRY(record_mark(events, 0, s));
+  const int32_t* sel = io->sel_tok;  // the kept set S_l that the rest of the layer reads
   if (selects) {
     CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, n_cand, plan->n_ctx, c.hkv, c.head_dim,
                                                io->dev, plan->err, s),
@@ -299,19 +301,21 @@ static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_i
                        "top-k"));
   } else {
     CB_TRY(record_mark(events, 1, s));
-    CB_TRY(cuda_status(cb::launch_copy_selection(cand, n_cand, io->sel_tok, io->sel_row, s), "selection copy"));
+    sel = cand;  // S_l = C_l: the fuse pass reads the candidates and copies them out
   }
   CB_TRY(record_mark(events, 2, s));
+  const bool copy_out = !selects && k > 0;
   CB_TRY(cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
-                                           io->sel_tok, k, plan->n_ctx, c.chunk_len, plan->n_tokens, c.hkv,
-                                           c.head_dim, c.rope_style, t, plan->err, s),
+                                           sel, k, copy_out ? io->sel_tok : nullptr,
+                                           copy_out ? io->sel_row : nullptr, plan->n_ctx, c.chunk_len,
+                                           plan->n_tokens, c.hkv, c.head_dim, c.rope_style, t, plan->err, s),
                      "fuse"));
   CB_TRY(record_mark(events, 3, s));
   if (mq == 0) {
     CB_TRY(record_mark(events, 4, s));
     return record_mark(events, 5, s);
   }
-  const cb::RowMap im{io->sel_tok, k, plan->n_ctx, plan->n_tokens};
+  const cb::RowMap im{sel, k, plan->n_ctx, plan->n_tokens};
   const cb::RowMap om{nullptr, mq, 0, mq};
   CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, plan->q_pos, mq, c.hq,
                                           c.head_dim, c.rope_style, t, plan->err, s),

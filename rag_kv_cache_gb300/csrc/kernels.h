@@ -45,11 +45,13 @@ cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new,
                                 cudaStream_t s);
 
 // One pass over all n_tokens rows: cached rows re-rotated by their chunk offset,
-// selected and suffix rows encoded from k_new / v_new.
+// selected and suffix rows encoded from k_new / v_new. With copy_tok set, the
+// list sel_tok[0..k) is also copied to copy_tok / copy_row (= 0..k-1).
 cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, const void* v_old,
                               const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
-                              int32_t n_ctx, int32_t chunk_len, int32_t n_tokens, int32_t hkv,
-                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s);
+                              int32_t* copy_tok, int32_t* copy_row, int32_t n_ctx, int32_t chunk_len,
+                              int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
+                              int32_t* err, cudaStream_t s);
 
 cudaError_t launch_copy_selection(const int32_t* cand, int32_t m, int32_t* sel_tok, int32_t* sel_row,
                                   cudaStream_t s);

@@ -35,10 +35,9 @@ __global__ void rope_table_kernel(float2* tab, int len, int half, int head_dim, 
 
 // Rotate one row of n_heads x D bf16 by the table row `cs` (sign of sin flipped when neg).
 // One warp per row; 16-byte accesses; src may equal dst.
-template <int STYLE>
+template <int STYLE, int B>
 __device__ __forceinline__ void rotate_row(uint8_t* dst, const uint8_t* src, int n_heads, int head_dim,
                                            const float2* __restrict__ cs, bool neg, int lane) {
-  constexpr int B = 4;
   if (STYLE == 0) {
     // pair (j, j + D/2): a unit is 8 consecutive j of one head, lo and hi halves.
     const int per_head = head_dim / 16;
@@ -130,6 +129,52 @@ __device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int b
   }
 }
 
+// Rotate pair-unit u of a row (half style: 8 frequencies of one head, lo and hi
+// halves; interleaved: one 16-byte vector = 4 pairs).
+template <int STYLE>
+__device__ __forceinline__ void rotate_unit(uint8_t* dst, const uint8_t* src, int u, int head_dim,
+                                            const float2* __restrict__ cs, bool neg) {
+  if (STYLE == 0) {
+    const int per_head = head_dim / 16;
+    const int h = u / per_head, c = u % per_head;
+    const size_t off = (size_t)h * head_dim * 2 + c * 16;
+    const uint4 lo = ld_stream(src + off), hi = ld_stream(src + off + head_dim);
+    float a[8], b[8], oa[8], ob[8];
+    unpack8(lo, a);
+    unpack8(hi, b);
+    const float4* t4 = reinterpret_cast<const float4*>(cs + c * 8);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 t = __ldg(t4 + e);
+      const float c0 = t.x, s0 = neg ? -t.y : t.y, c1 = t.z, s1 = neg ? -t.w : t.w;
+      oa[2 * e] = a[2 * e] * c0 - b[2 * e] * s0;
+      ob[2 * e] = a[2 * e] * s0 + b[2 * e] * c0;
+      oa[2 * e + 1] = a[2 * e + 1] * c1 - b[2 * e + 1] * s1;
+      ob[2 * e + 1] = a[2 * e + 1] * s1 + b[2 * e + 1] * c1;
+    }
+    st_stream(dst + off, pack8(oa));
+    st_stream(dst + off + head_dim, pack8(ob));
+  } else {
+    const int c = u % (head_dim / 8);
+    const uint4 v = ld_stream(src + (size_t)u * 16);
+    float a[8], o[8];
+    unpack8(v, a);
+    const float4* t4 = reinterpret_cast<const float4*>(cs + c * 4);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float4 t = __ldg(t4 + e);
+      const float c0 = t.x, s0 = neg ? -t.y : t.y, c1 = t.z, s1 = neg ? -t.w : t.w;
+      o[4 * e + 0] = a[4 * e + 0] * c0 - a[4 * e + 1] * s0;
+      o[4 * e + 1] = a[4 * e + 0] * s0 + a[4 * e + 1] * c0;
+      o[4 * e + 2] = a[4 * e + 2] * c1 - a[4 * e + 3] * s1;
+      o[4 * e + 3] = a[4 * e + 2] * s1 + a[4 * e + 3] * c1;
+    }
+    st_stream(dst + (size_t)u * 16, pack8(o));
+  }
+}
+
+// One warp per (row, group of 32 pair-units), one pair-unit per lane, so a wide
+// row (a query row of 32 heads) spreads over several warps.
 template <int STYLE>
 __global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint8_t* x, RowMap imap,
                                                         RowMap omap, const int32_t* pos_from,
@@ -137,27 +182,35 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint
                                                         int n_heads, int head_dim, RopeTable t,
                                                         int32_t* err) {
   const int lane = threadIdx.x % kWarp;
-  const int warps = gridDim.x * (blockDim.x / kWarp);
+  const int units = n_heads * head_dim / (STYLE == 0 ? 16 : 8);
+  const int per_row = (units + kWarp - 1) / kWarp;
+  const long long items = (long long)n * per_row;
+  const long long warps = (long long)gridDim.x * (blockDim.x / kWarp);
   const size_t row_bytes = (size_t)n_heads * head_dim * 2;
   const int half = head_dim / 2;
-  for (int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; i < n; i += warps) {
+  for (long long item = blockIdx.x * (long long)(blockDim.x / kWarp) + threadIdx.x / kWarp; item < items;
+       item += warps) {
+    const int i = (int)(item / per_row);
+    const int u = (int)(item % per_row) * kWarp + lane;
     const int src_row = map_row(imap, i);
     const int dst_row = map_row(omap, i);
     const int to = pos_to ? pos_to[i] : src_row;
     const int from = pos_from ? pos_from[i] : 0;
     const int delta = to - from;
     const int ad = delta < 0 ? -delta : delta;
-    if (pos_out && lane == 0) pos_out[i] = to;
+    const bool first = item % per_row == 0 && lane == 0;
+    if (pos_out && first) pos_out[i] = to;
     if (src_row < 0 || dst_row < 0 || src_row >= imap.limit || dst_row >= omap.limit) {
-      if (lane == 0) record_error(err, kErrIndex, i);
+      if (first) record_error(err, kErrIndex, i);
       continue;
     }
     if (ad >= t.len) {
-      if (lane == 0) record_error(err, kErrRopeRange, i);
+      if (first) record_error(err, kErrRopeRange, i);
       continue;
     }
-    rotate_row<STYLE>(out + dst_row * row_bytes, x + src_row * row_bytes, n_heads, head_dim,
-                      t.tab + (size_t)ad * half, delta < 0, lane);
+    if (u < units)
+      rotate_unit<STYLE>(out + dst_row * row_bytes, x + src_row * row_bytes, u, head_dim,
+                         t.tab + (size_t)ad * half, delta < 0);
   }
 }
 
@@ -344,62 +397,76 @@ __global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __
 }
 
 // ---------------------------------------------------------------------------
-// Fused cache: rows [r0, r0 + kRowsPerCta) per block, one warp per row.
-constexpr int kFuseRows = 16;
+// Fused cache: 8 consecutive rows per block, one warp per row.
+constexpr int kFuseRows = 8;
 constexpr int kFuseThreads = 256;
 
-// Mark the members of the ascending list sel[0..k) that fall in [r0, r0 + kFuseRows).
-__device__ __forceinline__ void mark_block(const int32_t* sel, int k, int r0, int n_ctx, uint8_t* is_sel,
-                                           int32_t* err) {
-  __shared__ int s_lo;
-  const int tid = threadIdx.x;
-  if (tid < kFuseRows) is_sel[tid] = 0;
-  if (tid == 0) {
-    int lo = 0, hi = k;  // first index with sel[idx] >= r0
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (sel[mid] < r0) lo = mid + 1; else hi = mid;
+// First index j in the ascending list sel[0..k) with sel[j] >= key (k if none),
+// by one warp: 32-ary search, one coalesced probe and ballot per round.
+__device__ __forceinline__ int warp_lower_bound(const int32_t* sel, int k, int key, int lane) {
+  int lo = 0, hi = k;  // the answer lies in [lo, hi]
+  while (hi - lo > kWarp) {
+    const int step = (hi - lo + kWarp - 1) / kWarp;
+    const int idx = lo + lane * step;
+    const unsigned less = __ballot_sync(0xffffffffu, idx < hi && sel[idx] < key);
+    const int c = __popc(less);  // probes below the answer form a prefix of the lanes
+    if (c == 0) {
+      hi = lo;
+      break;
     }
-    s_lo = lo;
+    const int nlo = lo + (c - 1) * step + 1;
+    hi = min(hi, lo + c * step);
+    lo = nlo;
   }
-  __syncthreads();
-  if (tid < kFuseRows) {
-    const int j = s_lo + tid;
-    if (j < k) {
-      const int t = sel[j];
-      if (t < 0 || t >= n_ctx) record_error(err, kErrIndex, j);
-      else if (j > 0 && sel[j - 1] >= t) record_error(err, kErrOrder, j);
-      else if (t < r0 + kFuseRows) is_sel[t - r0] = 1;
-    }
-  }
-  __syncthreads();
+  const int idx = lo + lane;
+  return lo + __popc(__ballot_sync(0xffffffffu, idx < hi && sel[idx] < key));
 }
 
 template <int STYLE>
 __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
     uint8_t* k_fused, uint8_t* v_fused, const uint8_t* k_old, const uint8_t* v_old, const uint8_t* k_new,
-    const uint8_t* v_new, const int32_t* sel, int k, int n_ctx, int chunk_len, int n_tokens, int hkv,
-    int head_dim, RopeTable t, int32_t* err) {
+    const uint8_t* v_new, const int32_t* sel, int k, int32_t* out_tok, int32_t* out_row, int n_ctx,
+    int chunk_len, int n_tokens, int hkv, int head_dim, RopeTable t, int32_t* err) {
   __shared__ uint8_t is_sel[kFuseRows];
-  const int r0 = blockIdx.x * kFuseRows;
-  mark_block(sel, k, r0, n_ctx, is_sel, err);
   const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
-  const size_t row_bytes = (size_t)hkv * head_dim * 2;
-  const int half = head_dim / 2;
-  for (int r = warp; r < kFuseRows; r += kFuseThreads / kWarp) {
-    const int tok = r0 + r;
-    if (tok >= n_tokens) break;
-    const bool fresh = tok >= n_ctx || is_sel[r];
-    const int pos = fresh ? tok : (tok / chunk_len) * chunk_len;  // encode at p, or move by the chunk start
-    if (pos >= t.len) {
-      if (lane == 0) record_error(err, kErrRopeRange, tok);
-      continue;
+  const int r0 = blockIdx.x * kFuseRows;
+  if (out_tok != nullptr && threadIdx.x < kFuseRows) {
+    // a layer that keeps its candidates: S = C is copied out alongside the pass
+    const int i = r0 + threadIdx.x;
+    if (i < k) {
+      out_tok[i] = sel[i];
+      out_row[i] = i;
     }
-    const uint8_t* ks = (fresh ? k_new : k_old) + tok * row_bytes;
-    const uint8_t* vs = (fresh ? v_new : v_old) + tok * row_bytes;
-    rotate_row<STYLE>(k_fused + tok * row_bytes, ks, hkv, head_dim, t.tab + (size_t)pos * half, false, lane);
-    copy_row(v_fused + tok * row_bytes, vs, (int)row_bytes, lane);
   }
+  if (warp == 0) {
+    const int j0 = warp_lower_bound(sel, k, r0, lane);
+    if (lane < kFuseRows) {
+      is_sel[lane] = 0;
+      __syncwarp(0xffu);
+      const int j = j0 + lane;
+      if (j < k) {
+        const int tk = sel[j];
+        if (tk < 0 || tk >= n_ctx) record_error(err, kErrIndex, j);
+        else if (j > 0 && sel[j - 1] >= tk) record_error(err, kErrOrder, j);
+        else if (tk < r0 + kFuseRows) is_sel[tk - r0] = 1;
+      }
+    }
+  }
+  __syncthreads();
+  const int tok = r0 + warp;
+  if (tok >= n_tokens) return;
+  const size_t row_bytes = (size_t)hkv * head_dim * 2;
+  const bool fresh = tok >= n_ctx || is_sel[warp];
+  const int pos = fresh ? tok : (tok / chunk_len) * chunk_len;  // encode at p, or move by the chunk start
+  if (pos >= t.len) {
+    if (lane == 0) record_error(err, kErrRopeRange, tok);
+    return;
+  }
+  const uint8_t* ks = (fresh ? k_new : k_old) + tok * row_bytes;
+  const uint8_t* vs = (fresh ? v_new : v_old) + tok * row_bytes;
+  rotate_row<STYLE, 2>(k_fused + tok * row_bytes, ks, hkv, head_dim, t.tab + (size_t)pos * (head_dim / 2), false,
+                       lane);
+  copy_row(v_fused + tok * row_bytes, vs, (int)row_bytes, lane);
 }
 
 template <int STYLE>
@@ -423,8 +490,8 @@ __global__ void __launch_bounds__(kFuseThreads) fuse_scatter_kernel(uint8_t* k_f
       if (lane == 0) record_error(err, kErrRopeRange, tok);
       continue;
     }
-    rotate_row<STYLE>(k_fused + tok * row_bytes, k_new + tok * row_bytes, hkv, head_dim,
-                      t.tab + (size_t)tok * half, false, lane);
+    rotate_row<STYLE, 2>(k_fused + tok * row_bytes, k_new + tok * row_bytes, hkv, head_dim,
+                         t.tab + (size_t)tok * half, false, lane);
     copy_row(v_fused + tok * row_bytes, v_new + tok * row_bytes, (int)row_bytes, lane);
   }
 }
@@ -457,7 +524,8 @@ cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap,
                              const int32_t* pos_to, int32_t* pos_out, int32_t n, int32_t n_heads,
                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  const int grid = grid_for_warps(n, 8);
+  const int units = n_heads * head_dim / (style == 0 ? 16 : 8);
+  const int grid = grid_for_warps((long long)n * ((units + kWarp - 1) / kWarp), 8);
   if (style == 0)
     rope_rows_kernel<0><<<grid, 256, 0, s>>>((uint8_t*)out, (const uint8_t*)x, imap, omap, pos_from, pos_to,
                                              pos_out, n, n_heads, head_dim, t, err);
@@ -511,8 +579,9 @@ cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new,
 
 cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, const void* v_old,
                               const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
-                              int32_t n_ctx, int32_t chunk_len, int32_t n_tokens, int32_t hkv,
-                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s) {
+                              int32_t* copy_tok, int32_t* copy_row, int32_t n_ctx, int32_t chunk_len,
+                              int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
+                              int32_t* err, cudaStream_t s) {
   if (n_tokens <= 0) return cudaSuccess;
   const int grid = (n_tokens + kFuseRows - 1) / kFuseRows;
   auto* kf = (uint8_t*)k_fused;
@@ -520,11 +589,13 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
   if (style == 0)
     blend_fuse_kernel<0><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
                                                        (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
-                                                       n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+                                                       copy_tok, copy_row, n_ctx, chunk_len, n_tokens, hkv,
+                                                       head_dim, t, err);
   else
     blend_fuse_kernel<1><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
                                                        (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
-                                                       n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+                                                       copy_tok, copy_row, n_ctx, chunk_len, n_tokens, hkv,
+                                                       head_dim, t, err);
   return cudaPeekAtLastError();
 }
 

@@ -260,3 +260,32 @@ def test_attention_peaked_scores_force_rescale(cb):
     q_pos = np.sort(rng.choice(1500, size=100, replace=False))
     got, ref = _attention_case(cb, 8, 2, 64, 1500, q_pos, seed=9, scale_q=6.0)
     assert_close_bf16(got, ref, what="peaked attention")
+
+
+def test_attention_score_jumps_past_the_overflow_guard(cb):
+    # Keys whose scores exceed everything earlier by far more than 2^64 (in base-2 units of the
+    # scaled score), in tiles handled by both softmax warpgroups: the one-pass softmax must move
+    # its reference (and the P values it already stored) instead of overflowing.
+    hq, hkv, d, n_keys = 8, 2, 128, 1000
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=n_keys - 1, n_suffix=1)
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(21)
+    q_pos = np.sort(np.concatenate([rng.choice(np.arange(0, 300), 20, replace=False),
+                                    rng.choice(np.arange(300, 700), 40, replace=False),
+                                    rng.choice(np.arange(700, n_keys), 40, replace=False)]))
+    mq = q_pos.size
+    q = f32_to_bf16_bits((1.0 + 0.1 * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    kf = rng.standard_normal((n_keys, hkv, d)).astype(np.float32)
+    kf[300] = 6.0   # tile 2 (even tiles)
+    kf[450] = 8.0   # tile 3 (odd tiles)
+    kf[705] = 12.0  # tile 5 (odd tiles), far above the tile-3 spike
+    k = f32_to_bf16_bits(kf)
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    got = bf16_bits_to_f64(bf16_bits(out))
+    assert np.all(np.isfinite(got))
+    assert_close_bf16(got, ref, what="attention with score jumps")
