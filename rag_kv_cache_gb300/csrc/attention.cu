@@ -54,6 +54,7 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t col_o(int b, int d) { return 256u + (uint32_t)(b * d); }
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr uint32_t kSuspendHintNs = 200000;  // a sleeping waiter re-checks abort and time at least this often
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 constexpr float kOverflowGuard = 64.0f;    // log2 units: largest exponent the one-pass softmax accepts
 
@@ -117,13 +118,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Slow path of mbar_wait: spin with a time limit.
+// try_wait that lets the thread sleep (up to the hint, in ns) until the phase completes, so
+// waiting warps do not take issue slots from the softmax warps on their sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Slow path of mbar_wait: sleep-wait with a time limit.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                             int site, bool honour_abort) {
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((n & 7u) == 0) {
       if (honour_abort && *abort_flag) return false;
       if (global_timer() - t0 > kTimeoutNs) {
         *abort_flag = 1;
@@ -190,6 +205,26 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (sm_100 family f32x2 arithmetic: two lanes per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (8-row x 128-byte atoms).
@@ -455,9 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exponentials: every exponent at most kOverflowGuard keeps P and the fp32 sums finite.
         // P chunk ch (keys 32ch..) is stored in columns 16ch..16ch+15, which hold keys already read.
         float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;  // reference 0 while nothing was visible
-        float pm[8], ps[8];
+        float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        uint64_t ps2[4];  // partial row sums, packed pairs
 #pragma unroll
-        for (int q = 0; q < 8; ++q) pm[q] = -INFINITY, ps[q] = 0.0f;
+        for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
         int bail = 4;  // first chunk that failed the guard
         {
           uint32_t ca[32], cb[32];
@@ -469,27 +505,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
             if (ch < 3) tmem_ld_x32_async(s_addr + (ch + 1) * 32, nxt);
             if (bail == 4) {  // warp-uniform
-              float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+              if (masking) {  // diagonal tiles only: hide the keys past this row's position
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(cur[c]);
-                cm[c & 3] = fmaxf(cm[c & 3], v);
+                for (int c = 0; c < 32; ++c)
+                  if (ch * 32 + c > lim) cur[c] = 0xff800000u;  // -inf
               }
-              const float cmax = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-              if (__any_sync(0xffffffffu, cmax * p.scale_log2 + neg_m > kOverflowGuard)) {
-                bail = ch;
+              // Exponent arguments t = s * scale - m and their exponentials first; the guard on
+              // max t is voted while the exponentials are in flight, and P is stored only if it holds.
+              const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
+              float pv[32];
+              float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float t0, t1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sc2, nm2),
+                          t0, t1);
+                pv[2 * e] = ex2(t0);
+                pv[2 * e + 1] = ex2(t1);
+                tm[e & 3] = fmaxf(tm[e & 3], fmaxf(t0, t1));
+              }
+              const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+              if (__any_sync(0xffffffffu, tmax > kOverflowGuard)) {
+                bail = ch;  // nothing of this chunk was stored: its S columns are intact
               } else {
-                pm[ch] = cmax;
+                pm[ch] = tmax;
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                  const float v0 = (masking && ch * 32 + 2 * e > lim) ? -INFINITY : __uint_as_float(cur[2 * e]);
-                  const float v1 =
-                      (masking && ch * 32 + 2 * e + 1 > lim) ? -INFINITY : __uint_as_float(cur[2 * e + 1]);
-                  const float p0 = ex2(fmaf(v0, p.scale_log2, neg_m));
-                  const float p1 = ex2(fmaf(v1, p.scale_log2, neg_m));
-                  ps[e & 7] += p0 + p1;
-                  pk[e] = pack2(p0, p1);
+                  ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(pv[2 * e], pv[2 * e + 1]));
+                  pk[e] = pack2(pv[2 * e], pv[2 * e + 1]);
                 }
                 tmem_st_x16(s_addr + ch * 16, pk);
               }
@@ -497,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ch < 3) tmem_wait_ld(nxt);
           }
         }
-        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * p.scale_log2;
+        // row max of the scaled scores seen in this tile (pm holds max t = s * scale - m)
+        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) - neg_m;
         if (bail < 4) {
           // Rare: a row's max jumped past the guard at chunk `bail`. Chunks bail.. are intact in
           // TMEM; find the tile's max, move O, l, the partial sums and the P chunks already
@@ -523,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) ps[q] *= beta;
+          for (int q = 0; q < 4; ++q) ps2[q] = f2_fma(ps2[q], f2_pack(beta, beta), f2_pack(0.0f, 0.0f));
 #pragma unroll 1
           for (int ch = 0; ch < bail; ++ch) {
             uint32_t q16[16];
@@ -545,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float v1 = (masking && ch * 32 + 2 * e + 1 > lim) ? -INFINITY : __uint_as_float(c32[2 * e + 1]);
               const float p0 = ex2(fmaf(v0, p.scale_log2, neg_m));
               const float p1 = ex2(fmaf(v1, p.scale_log2, neg_m));
-              ps[e & 7] += p0 + p1;
+              ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
               pk[e] = pack2(p0, p1);
             }
             tmem_st_x16(s_addr + ch * 16, pk);
@@ -553,7 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (m_ref == -INFINITY && mx > -INFINITY) {
           m_ref = 0.0f;  // this pass used reference 0
         }
-        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        float sa, sb;
+        f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa, sb);
+        l += sa + sb;
         m_seen = fmaxf(m_seen, mx);
       }
       tmem_st_wait();
