@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK0 = base + kQBytes;
   const uint32_t sV0 = sK0 + kKStages * kKVBytes;
 
+  pdl_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int lin = blockIdx.x;
   const int tile = p.n_qtiles - 1 - lin / p.hkv;  // later (longer) query tiles first
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();  // the query rows, positions and fused K/V come from the kernels before this one
 
   // Query position of each softmax thread's row; padded rows repeat the tile's last token.
   int my_pos = 0;
@@ -721,8 +723,7 @@ cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  hkvd_attention_kernel<D><<<n_qtiles * hkv, kThreads, smem, s>>>(tq_map, tk_map, tv_map, p);
-  return cudaPeekAtLastError();
+  return launch_pdl(hkvd_attention_kernel<D>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map, p);
 }
 
 }  // namespace

@@ -53,8 +53,6 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
                               int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
                               int32_t* err, cudaStream_t s);
 
-cudaError_t launch_copy_selection(const int32_t* cand, int32_t m, int32_t* sel_tok, int32_t* sel_row,
-                                  cudaStream_t s);
 
 // Causal GQA attention over compact RoPE-encoded query rows.
 cudaError_t launch_hkvd_attention(const void* q, const int32_t* q_pos, int32_t mq, const void* k,

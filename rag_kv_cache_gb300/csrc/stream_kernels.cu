@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint
                                                         const int32_t* pos_to, int32_t* pos_out, int n,
                                                         int n_heads, int head_dim, RopeTable t,
                                                         int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const int units = n_heads * head_dim / (STYLE == 0 ? 16 : 8);
   const int per_row = (units + kWarp - 1) / kWarp;
@@ -221,6 +223,8 @@ template <int CPL>  // chunks per lane (ceil(E / 256))
 __global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* v_new, const uint8_t* v_old,
                                                            const int32_t* cand, int m, int n_rows,
                                                            int elems, float* dev, int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
   if (i >= m) return;
@@ -279,6 +283,8 @@ __global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __
                                                                   const int32_t* __restrict__ cand, int m,
                                                                   int k, int32_t* sel_tok, int32_t* sel_row,
                                                                   int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_remaining;
@@ -427,6 +433,8 @@ __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
     uint8_t* k_fused, uint8_t* v_fused, const uint8_t* k_old, const uint8_t* v_old, const uint8_t* k_new,
     const uint8_t* v_new, const int32_t* sel, int k, int32_t* out_tok, int32_t* out_row, int n_ctx,
     int chunk_len, int n_tokens, int hkv, int head_dim, RopeTable t, int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ uint8_t is_sel[kFuseRows];
   const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
   const int r0 = blockIdx.x * kFuseRows;
@@ -475,6 +483,8 @@ __global__ void __launch_bounds__(kFuseThreads) fuse_scatter_kernel(uint8_t* k_f
                                                                     const int32_t* sel, int k, int n_ctx,
                                                                     int n_tokens, int hkv, int head_dim,
                                                                     RopeTable t, int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x % kWarp;
   const int warps = gridDim.x * (blockDim.x / kWarp);
   const int rows = k + (n_tokens - n_ctx);
@@ -493,13 +503,6 @@ __global__ void __launch_bounds__(kFuseThreads) fuse_scatter_kernel(uint8_t* k_f
     rotate_row<STYLE, 2>(k_fused + tok * row_bytes, k_new + tok * row_bytes, hkv, head_dim,
                          t.tab + (size_t)tok * half, false, lane);
     copy_row(v_fused + tok * row_bytes, v_new + tok * row_bytes, (int)row_bytes, lane);
-  }
-}
-
-__global__ void copy_selection_kernel(const int32_t* cand, int m, int32_t* sel_tok, int32_t* sel_row) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < m; i += gridDim.x * blockDim.x) {
-    sel_tok[i] = cand ? cand[i] : i;
-    sel_row[i] = i;
   }
 }
 
@@ -527,11 +530,11 @@ cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap,
   const int units = n_heads * head_dim / (style == 0 ? 16 : 8);
   const int grid = grid_for_warps((long long)n * ((units + kWarp - 1) / kWarp), 8);
   if (style == 0)
-    rope_rows_kernel<0><<<grid, 256, 0, s>>>((uint8_t*)out, (const uint8_t*)x, imap, omap, pos_from, pos_to,
-                                             pos_out, n, n_heads, head_dim, t, err);
+    return launch_pdl(rope_rows_kernel<0>, grid, 256, 0, s, (uint8_t*)out, (const uint8_t*)x, imap, omap,
+                      pos_from, pos_to, pos_out, n, n_heads, head_dim, t, err);
   else
-    rope_rows_kernel<1><<<grid, 256, 0, s>>>((uint8_t*)out, (const uint8_t*)x, imap, omap, pos_from, pos_to,
-                                             pos_out, n, n_heads, head_dim, t, err);
+    return launch_pdl(rope_rows_kernel<1>, grid, 256, 0, s, (uint8_t*)out, (const uint8_t*)x, imap, omap,
+                      pos_from, pos_to, pos_out, n, n_heads, head_dim, t, err);
   return cudaPeekAtLastError();
 }
 
@@ -544,19 +547,17 @@ cudaError_t launch_kv_deviation(const void* v_new, const void* v_old, const int3
   const int grid = (m + 7) / 8;
   const uint8_t* a = (const uint8_t*)v_new;
   const uint8_t* b = (const uint8_t*)v_old;
-  if (cpl <= 1) kv_deviation_kernel<1><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
-  else if (cpl <= 2) kv_deviation_kernel<2><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
-  else if (cpl <= 4) kv_deviation_kernel<4><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
-  else if (cpl <= 8) kv_deviation_kernel<8><<<grid, 256, 0, s>>>(a, b, cand, m, n_rows, elems, dev, err);
-  else return cudaErrorInvalidValue;
-  return cudaPeekAtLastError();
+  if (cpl <= 1) return launch_pdl(kv_deviation_kernel<1>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
+  if (cpl <= 2) return launch_pdl(kv_deviation_kernel<2>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
+  if (cpl <= 4) return launch_pdl(kv_deviation_kernel<4>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
+  if (cpl <= 8) return launch_pdl(kv_deviation_kernel<8>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,
                              int32_t* sel_row, int32_t* err, cudaStream_t s) {
   if (k <= 0 || m <= 0) return cudaSuccess;
-  hkvd_topk_kernel<<<1, kTopkThreads, 0, s>>>(dev, cand, m, k, sel_tok, sel_row, err);
-  return cudaPeekAtLastError();
+  return launch_pdl(hkvd_topk_kernel, 1, kTopkThreads, 0, s, dev, cand, m, k, sel_tok, sel_row, err);
 }
 
 cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new, const void* v_new,
@@ -567,13 +568,13 @@ cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new,
   if (rows <= 0) return cudaSuccess;
   const int grid = grid_for_warps(rows, kFuseThreads / kWarp);
   if (style == 0)
-    fuse_scatter_kernel<0><<<grid, kFuseThreads, 0, s>>>((uint8_t*)k_fused, (uint8_t*)v_fused,
-                                                         (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok,
-                                                         k, n_ctx, n_tokens, hkv, head_dim, t, err);
+    return launch_pdl(fuse_scatter_kernel<0>, grid, kFuseThreads, 0, s, (uint8_t*)k_fused, (uint8_t*)v_fused,
+                      (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, n_ctx, n_tokens, hkv, head_dim, t,
+                      err);
   else
-    fuse_scatter_kernel<1><<<grid, kFuseThreads, 0, s>>>((uint8_t*)k_fused, (uint8_t*)v_fused,
-                                                         (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok,
-                                                         k, n_ctx, n_tokens, hkv, head_dim, t, err);
+    return launch_pdl(fuse_scatter_kernel<1>, grid, kFuseThreads, 0, s, (uint8_t*)k_fused, (uint8_t*)v_fused,
+                      (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, n_ctx, n_tokens, hkv, head_dim, t,
+                      err);
   return cudaPeekAtLastError();
 }
 
@@ -587,23 +588,15 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
   auto* kf = (uint8_t*)k_fused;
   auto* vf = (uint8_t*)v_fused;
   if (style == 0)
-    blend_fuse_kernel<0><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
-                                                       (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
-                                                       copy_tok, copy_row, n_ctx, chunk_len, n_tokens, hkv,
-                                                       head_dim, t, err);
+    return launch_pdl(blend_fuse_kernel<0>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
+                      (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
+                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
   else
-    blend_fuse_kernel<1><<<grid, kFuseThreads, 0, s>>>(kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
-                                                       (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k,
-                                                       copy_tok, copy_row, n_ctx, chunk_len, n_tokens, hkv,
-                                                       head_dim, t, err);
+    return launch_pdl(blend_fuse_kernel<1>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
+                      (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
+                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
   return cudaPeekAtLastError();
 }
 
-cudaError_t launch_copy_selection(const int32_t* cand, int32_t m, int32_t* sel_tok, int32_t* sel_row,
-                                  cudaStream_t s) {
-  if (m <= 0) return cudaSuccess;
-  copy_selection_kernel<<<(m + 255) / 256, 256, 0, s>>>(cand, m, sel_tok, sel_row);
-  return cudaPeekAtLastError();
-}
 
 }  // namespace cb
