@@ -85,8 +85,8 @@ typedef struct cb_config {
 typedef struct cb_plan cb_plan;
 
 /* Create a plan on the current device: copies *cfg, builds the RoPE cos/sin
- * table for positions 0 .. n_tokens-1 (fp64 angles rounded to fp32) and the
- * scratch the per-layer driver needs. Synchronous. */
+ * table for positions 0 .. n_tokens-1 (fp64 angles rounded to fp32), the
+ * device error word and the side streams of cb_blend_request. Synchronous. */
 cb_status cb_plan_create(const cb_config* cfg, cb_plan** out);
 
 /* Free everything the plan owns. Waits for the device first. NULL is a no-op. */
@@ -179,6 +179,19 @@ typedef struct cb_layer_io {
  *   by their chunk offset, S_l and suffix rows encoded from k_new / v_new),
  *   the query rows encoded, and the attention. */
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream);
+
+/* All layers 1..n_layers of one request (ios[l-1] = buffers of layer l) with
+ * the gradual filter wired automatically: layer l reads the candidates
+ * ios[l-2].sel_tok (ios[].cand is ignored). Same results as calling
+ * cb_blend_layer for each layer in order, but scheduled over streams the plan
+ * owns: every layer's deviation, top-k, fused-cache and query-encoding kernels
+ * run on one side stream, ahead of the attention, and the attention of
+ * consecutive layers runs on two streams, so that one layer's attention
+ * overlaps the next layer's streaming kernels and the tail of the previous
+ * attention. All work is ordered after prior work on `stream` and completes
+ * before later work on it. The layers' buffers must not alias one another.
+ * Capturable into a CUDA graph on `stream`. */
+cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios, void* stream);
 
 /* cb_blend_layer with timing marks: events[0..5] are cudaEvent_t handles (any
  * may be NULL) recorded on `stream` before the deviation, before the top-k,

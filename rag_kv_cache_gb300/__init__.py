@@ -16,7 +16,8 @@ from . import _lib
 from ._lib import CacheBlendError, check
 
 __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_hkvd_topk", "cb_fuse_scatter",
-           "cb_hkvd_attention", "cb_blend_layer", "cb_check", "cb_version", "LayerBuffers"]
+           "cb_hkvd_attention", "cb_blend_layer", "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check",
+           "cb_version", "LayerBuffers"]
 
 
 def _ptr(t, dtype=None, name="tensor"):
@@ -159,6 +160,27 @@ class LayerBuffers:
         self.out = torch.empty(max(mq1, 1), plan.hq, plan.head_dim, **bf)
 
 
+def _layer_io(k_old, v_old, k_new, v_new, q, cand, bufs):
+    return _lib.CbLayerIO(
+        _ptr(k_old, torch.bfloat16, "k_old"), _ptr(v_old, torch.bfloat16, "v_old"),
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(cand, torch.int32, "cand"), _ptr(bufs.dev, torch.float32, "dev"),
+        _ptr(bufs.sel_tok, torch.int32, "sel_tok"), _ptr(bufs.sel_row, torch.int32, "sel_row"),
+        _ptr(bufs.k_fused, torch.bfloat16, "k_fused"), _ptr(bufs.v_fused, torch.bfloat16, "v_fused"),
+        _ptr(bufs.q_rot, torch.bfloat16, "q_rot"), _ptr(bufs.out, torch.bfloat16, "out"))
+
+
+def cb_blend_request(plan, layers, stream=None):
+    """All layers of one request (cb_blend_request): `layers` lists, for layers 1..n, dicts with
+    k_old, v_old, k_new, v_new, q and bufs (a LayerBuffers per layer; buffers must not alias).
+    Layer l reads the candidates layers[l-2]["bufs"].sel_tok."""
+    n = len(layers)
+    arr = (_lib.CbLayerIO * n)()
+    for i, L in enumerate(layers):
+        arr[i] = _layer_io(L["k_old"], L["v_old"], L["k_new"], L["v_new"], L["q"], None, L["bufs"])
+    check(_lib.load().cb_blend_request(plan.handle, n, arr, _stream(stream)))
+
+
 def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None,
                    events=None):
     """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer)).
@@ -167,13 +189,7 @@ def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: La
     boundaries (cb_blend_layer_timed); each event must have been recorded once before
     so that its CUDA handle exists.
     """
-    io = _lib.CbLayerIO(
-        _ptr(k_old, torch.bfloat16, "k_old"), _ptr(v_old, torch.bfloat16, "v_old"),
-        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
-        _ptr(q, torch.bfloat16, "q"), _ptr(cand, torch.int32, "cand"), _ptr(bufs.dev, torch.float32, "dev"),
-        _ptr(bufs.sel_tok, torch.int32, "sel_tok"), _ptr(bufs.sel_row, torch.int32, "sel_row"),
-        _ptr(bufs.k_fused, torch.bfloat16, "k_fused"), _ptr(bufs.v_fused, torch.bfloat16, "v_fused"),
-        _ptr(bufs.q_rot, torch.bfloat16, "q_rot"), _ptr(bufs.out, torch.bfloat16, "out"))
+    io = _layer_io(k_old, v_old, k_new, v_new, q, cand, bufs)
     if events is None:
         check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))
         return

@@ -71,7 +71,11 @@ struct Bars {
 };
 
 struct Params {
-  const int32_t* q_pos;
+  // Position of query row t: t < pos_k ? pos_idx[t] : pos_base + (t - pos_k).
+  const int32_t* pos_idx;
+  int pos_k;
+  int pos_base;
+  int wait_prior;  // 1: wait for the previous kernel on the stream before reading (programmatic launch)
   int mq;
   int n_keys;
   int hq;
@@ -304,20 +308,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   __syncthreads();
-  pdl_wait();  // the query rows, positions and fused K/V come from the kernels before this one
+  // The query rows, positions and fused K/V come from the kernels before this one on the stream,
+  // unless the caller orders them by other means (events) and lets this kernel overlap its
+  // same-stream predecessor.
+  if (p.wait_prior) pdl_wait();
 
   // Query position of each softmax thread's row; padded rows repeat the tile's last token.
   int my_pos = 0;
   if (threadIdx.x < 2 * kSoftmaxThreads) {
     const int r = threadIdx.x % kBM;
     const int t = min(t0 + r / p.group, t_last);
-    int pos = p.q_pos[t];
+    auto qpos = [&](int tt) { return tt < p.pos_k ? p.pos_idx[tt] : p.pos_base + (tt - p.pos_k); };
+    int pos = qpos(t);
     if (pos < 0 || pos >= p.n_keys) {
       if (threadIdx.x < kSoftmaxThreads) record_error(p.err, kErrIndex, t);
       pos = pos < 0 ? 0 : p.n_keys - 1;
     }
     if (threadIdx.x < kSoftmaxThreads) {
-      if (r % p.group == 0 && t == t0 + r / p.group && t > 0 && p.q_pos[t - 1] >= p.q_pos[t])
+      if (r % p.group == 0 && t == t0 + r / p.group && t > 0 && qpos(t - 1) >= pos)
         record_error(p.err, kErrOrder, t);
       atomicMax(&s_maxpos, pos);
     }
@@ -687,7 +695,7 @@ bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* 
 }
 
 template <int D>
-cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void* k, const void* v, int n_keys,
+cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k, const void* v, int n_keys,
                          int hq, int hkv, float scale, void* out, int32_t* err, cudaStream_t s) {
   const int group = hq / hkv;
   const int tq = kBM / group;
@@ -703,7 +711,10 @@ cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void
       !encode_map(&tv_map, v, 3, kd, ks, kbx))
     return cudaErrorInvalidValue;
   Params p;
-  p.q_pos = q_pos;
+  p.pos_idx = qp.idx;
+  p.pos_k = qp.k;
+  p.pos_base = qp.base;
+  p.wait_prior = qp.wait_prior ? 1 : 0;
   p.mq = mq;
   p.n_keys = n_keys;
   p.hq = hq;
@@ -728,12 +739,12 @@ cudaError_t launch_typed(const void* q, const int32_t* q_pos, int mq, const void
 
 }  // namespace
 
-cudaError_t launch_hkvd_attention(const void* q, const int32_t* q_pos, int32_t mq, const void* k, const void* v,
+cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, const void* k, const void* v,
                                   int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim, float scale, void* out,
                                   int32_t* err, cudaStream_t s) {
   if (mq <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_typed<128>(q, q_pos, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
-  if (head_dim == 64) return launch_typed<64>(q, q_pos, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+  if (head_dim == 128) return launch_typed<128>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+  if (head_dim == 64) return launch_typed<64>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
   return cudaErrorInvalidValue;
 }
 

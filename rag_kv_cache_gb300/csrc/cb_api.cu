@@ -18,7 +18,9 @@ struct cb_plan {
   int32_t n_tokens;
   float2* rope_tab;  // [n_tokens][head_dim / 2]
   int32_t* err;      // [0] flags, [1] first offending index (-1 = none)
-  int32_t* q_pos;    // [n_tokens] positions of the encoded query rows of the current layer
+  cudaStream_t aux_stream;  // cb_blend_request: every layer's deviation, top-k, fuse and query encoding
+  cudaStream_t aux_attn;    // cb_blend_request: attention of even layers (odd layers on the caller's stream)
+  cudaEvent_t ev_fork, ev_ready, ev_join;
 };
 
 namespace {
@@ -111,7 +113,11 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess) e = cudaMalloc(&p->rope_tab, sizeof(float2) * (size_t)n_tokens * (c.head_dim / 2));
   if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&p->q_pos, sizeof(int32_t) * (size_t)n_tokens);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux_attn, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
 
   if (e == cudaSuccess) {
     const int32_t init[2] = {0, -1};
@@ -132,7 +138,11 @@ cb_status cb_plan_destroy(cb_plan* plan) {
   cudaDeviceSynchronize();
   cudaFree(plan->rope_tab);
   cudaFree(plan->err);
-  cudaFree(plan->q_pos);
+  if (plan->aux_stream) cudaStreamDestroy(plan->aux_stream);
+  if (plan->aux_attn) cudaStreamDestroy(plan->aux_attn);
+  if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
+  if (plan->ev_ready) cudaEventDestroy(plan->ev_ready);
+  if (plan->ev_join) cudaEventDestroy(plan->ev_join);
   delete plan;
   return CB_OK;
 }
@@ -234,22 +244,11 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
   CB_TRY(need_tensor(v, "v"));
   CB_TRY(need_tensor(out, "out"));
   if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)plan->cfg.head_dim);
-  return cuda_status(cb::launch_hkvd_attention(q, q_pos, mq, k, v, n_keys, plan->cfg.hq, plan->cfg.hkv,
+  const cb::QueryPositions qp{q_pos, mq, 0, true};
+  return cuda_status(cb::launch_hkvd_attention(q, qp, mq, k, v, n_keys, plan->cfg.hq, plan->cfg.hkv,
                                                plan->cfg.head_dim, scale, out, plan->err,
                                                static_cast<cudaStream_t>(stream)),
                      "cb_hkvd_attention");
-}
-
-static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                                  void* const* events);
-
-cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
-  return blend_layer_impl(plan, layer, io, stream, nullptr);
-}
-
-cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                               void* const* events) {
-  return blend_layer_impl(plan, layer, io, stream, events);
 }
 
 static cb_status record_mark(void* const* events, int i, cudaStream_t s) {
@@ -262,12 +261,15 @@ static cb_status record_mark(void* const* events, int i, cudaStream_t s) {
   return cuda_status(e, "stage event");
 }
 
-static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                                  void* const* events) {
-  CB_TRY(check_plan(plan));
-  CB_TRY(need_ptr(io, "io"));
+struct LayerShape {
   int32_t n_cand, k, mq, selects;
-  CB_TRY(cb_layer_sizes(plan, layer, &n_cand, &k, &mq, &selects));
+};
+
+// Host checks of one layer's buffers; `cand` is the candidate list the layer will read.
+static cb_status validate_io(cb_plan* plan, int32_t layer, const cb_layer_io* io, const int32_t* cand,
+                             LayerShape* sh) {
+  CB_TRY(need_ptr(io, "io"));
+  CB_TRY(cb_layer_sizes(plan, layer, &sh->n_cand, &sh->k, &sh->mq, &sh->selects));
   CB_TRY(need_tensor(io->k_old, "io.k_old"));
   CB_TRY(need_tensor(io->v_old, "io.v_old"));
   CB_TRY(need_tensor(io->k_new, "io.k_new"));
@@ -275,57 +277,122 @@ static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_i
   CB_TRY(need_tensor(io->q, "io.q"));
   CB_TRY(need_tensor(io->k_fused, "io.k_fused"));
   CB_TRY(need_tensor(io->v_fused, "io.v_fused"));
-  if (mq > 0) {
+  if (sh->mq > 0) {
     CB_TRY(need_tensor(io->q_rot, "io.q_rot"));
     CB_TRY(need_tensor(io->out, "io.out"));
   }
-  if (k > 0) {
+  if (sh->k > 0) {
     CB_TRY(need_ptr(io->sel_tok, "io.sel_tok"));
     CB_TRY(need_ptr(io->sel_row, "io.sel_row"));
   }
-  if (layer >= 2 && n_cand > 0) CB_TRY(need_ptr(io->cand, "io.cand"));
-  if (selects && n_cand > 0) CB_TRY(need_ptr(io->dev, "io.dev"));
-  const auto& c = plan->cfg;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cb::RopeTable t = table(plan);
-  const int32_t* cand = layer == 1 ? nullptr : io->cand;
+  if (layer >= 2 && sh->n_cand > 0) CB_TRY(need_ptr(cand, "io.cand"));
+  if (sh->selects && sh->n_cand > 0) CB_TRY(need_ptr(io->dev, "io.dev"));
+  return CB_OK;
+}
 
+// Deviation + top-k (selecting layers), fused cache and query encoding of one layer on `s`.
+// Returns the list S_l the layer's attention reads (`*sel`).
+static cb_status enqueue_streaming(cb_plan* plan, int32_t layer, const cb_layer_io* io, const int32_t* cand,
+                                   const LayerShape& sh, cudaStream_t s, void* const* events, const int32_t** sel_out) {
+  const auto& c = plan->cfg;
+  const cb::RopeTable t = table(plan);
+  if (layer == 1) cand = nullptr;
   CB_TRY(record_mark(events, 0, s));
-  const int32_t* sel = io->sel_tok;  // the kept set S_l that the rest of the layer reads
-  if (selects) {
-    CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, n_cand, plan->n_ctx, c.hkv, c.head_dim,
-                                               io->dev, plan->err, s),
+  const int32_t* sel = io->sel_tok;
+  if (sh.selects) {
+    CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, sh.n_cand, plan->n_ctx, c.hkv,
+                                               c.head_dim, io->dev, plan->err, s),
                        "deviation"));
     CB_TRY(record_mark(events, 1, s));
-    CB_TRY(cuda_status(cb::launch_hkvd_topk(io->dev, cand, n_cand, k, io->sel_tok, io->sel_row, plan->err, s),
+    CB_TRY(cuda_status(cb::launch_hkvd_topk(io->dev, cand, sh.n_cand, sh.k, io->sel_tok, io->sel_row, plan->err, s),
                        "top-k"));
   } else {
     CB_TRY(record_mark(events, 1, s));
     sel = cand;  // S_l = C_l: the fuse pass reads the candidates and copies them out
   }
   CB_TRY(record_mark(events, 2, s));
-  const bool copy_out = !selects && k > 0;
+  const bool copy_out = !sh.selects && sh.k > 0;
   CB_TRY(cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
-                                           sel, k, copy_out ? io->sel_tok : nullptr,
+                                           sel, sh.k, copy_out ? io->sel_tok : nullptr,
                                            copy_out ? io->sel_row : nullptr, plan->n_ctx, c.chunk_len,
                                            plan->n_tokens, c.hkv, c.head_dim, c.rope_style, t, plan->err, s),
                      "fuse"));
   CB_TRY(record_mark(events, 3, s));
-  if (mq == 0) {
-    CB_TRY(record_mark(events, 4, s));
-    return record_mark(events, 5, s);
+  if (sh.mq > 0) {
+    const cb::RowMap im{sel, sh.k, plan->n_ctx, plan->n_tokens};
+    const cb::RowMap om{nullptr, sh.mq, 0, sh.mq};
+    CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, nullptr, sh.mq, c.hq,
+                                            c.head_dim, c.rope_style, t, plan->err, s),
+                       "query encode"));
   }
-  const cb::RowMap im{sel, k, plan->n_ctx, plan->n_tokens};
-  const cb::RowMap om{nullptr, mq, 0, mq};
-  CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, plan->q_pos, mq, c.hq,
-                                          c.head_dim, c.rope_style, t, plan->err, s),
-                     "query encode"));
+  *sel_out = sel;
+  return CB_OK;
+}
+
+// The layer's attention on `s`: query row t sits at sel[t] (t < k) or n_ctx + t - k.
+static cb_status enqueue_attention(cb_plan* plan, const cb_layer_io* io, const int32_t* sel, const LayerShape& sh,
+                                   cudaStream_t s, void* const* events) {
+  const auto& c = plan->cfg;
   CB_TRY(record_mark(events, 4, s));
-  CB_TRY(cuda_status(cb::launch_hkvd_attention(io->q_rot, plan->q_pos, mq, io->k_fused, io->v_fused, plan->n_tokens,
-                                               c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
-                                               io->out, plan->err, s),
-                     "attention"));
+  if (sh.mq > 0) {
+    const cb::QueryPositions qp{sel, sh.k, plan->n_ctx, true};
+    CB_TRY(cuda_status(cb::launch_hkvd_attention(io->q_rot, qp, sh.mq, io->k_fused, io->v_fused, plan->n_tokens,
+                                                 c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
+                                                 io->out, plan->err, s),
+                       "attention"));
+  }
   return record_mark(events, 5, s);
+}
+
+static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                                  void* const* events) {
+  CB_TRY(check_plan(plan));
+  LayerShape sh;
+  CB_TRY(validate_io(plan, layer, io, io ? io->cand : nullptr, &sh));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t* sel = nullptr;
+  CB_TRY(enqueue_streaming(plan, layer, io, io->cand, sh, s, events, &sel));
+  return enqueue_attention(plan, io, sel, sh, s, events);
+}
+
+cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
+  return blend_layer_impl(plan, layer, io, stream, nullptr);
+}
+
+cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
+                               void* const* events) {
+  return blend_layer_impl(plan, layer, io, stream, events);
+}
+
+cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (n_layers < 1) return fail(CB_ERR_INVALID_ARG, "n_layers must be >= 1");
+  CB_TRY(need_ptr(ios, "ios"));
+  for (int32_t l = 1; l <= n_layers; ++l) {
+    LayerShape sh;
+    CB_TRY(validate_io(plan, l, &ios[l - 1], l == 1 ? nullptr : ios[l - 2].sel_tok, &sh));
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t attn_stream[2] = {s, plan->aux_attn};
+  CB_TRY(cuda_status(cudaEventRecord(plan->ev_fork, s), "fork"));
+  CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_stream, plan->ev_fork, 0), "fork"));
+  CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_attn, plan->ev_fork, 0), "fork"));
+  for (int32_t l = 1; l <= n_layers; ++l) {
+    const cb_layer_io* io = &ios[l - 1];
+    LayerShape sh;
+    CB_TRY(validate_io(plan, l, io, l == 1 ? nullptr : ios[l - 2].sel_tok, &sh));
+    const int32_t* sel = nullptr;
+    CB_TRY(enqueue_streaming(plan, l, io, l == 1 ? nullptr : ios[l - 2].sel_tok, sh, plan->aux_stream, nullptr,
+                             &sel));
+    const cudaStream_t a = attn_stream[(l - 1) & 1];
+    CB_TRY(cuda_status(cudaEventRecord(plan->ev_ready, plan->aux_stream), "layer inputs ready"));
+    CB_TRY(cuda_status(cudaStreamWaitEvent(a, plan->ev_ready, 0), "layer inputs ready"));
+    CB_TRY(enqueue_attention(plan, io, sel, sh, a, nullptr));
+  }
+  CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, plan->aux_attn), "join"));
+  CB_TRY(cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join"));
+  CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, plan->aux_stream), "join"));
+  return cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join");
 }
 
 cb_status cb_check(cb_plan* plan) {

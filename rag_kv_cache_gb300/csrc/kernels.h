@@ -54,8 +54,18 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
                               int32_t* err, cudaStream_t s);
 
 
+// Positions of the compact query rows: row t < k sits at idx[t], row t >= k at base + (t - k).
+// wait_prior: the kernel waits for its predecessor on the stream (programmatic launch) before
+// reading; false when the caller orders its inputs by events and allows the overlap.
+struct QueryPositions {
+  const int32_t* idx;
+  int32_t k;
+  int32_t base;
+  bool wait_prior;
+};
+
 // Causal GQA attention over compact RoPE-encoded query rows.
-cudaError_t launch_hkvd_attention(const void* q, const int32_t* q_pos, int32_t mq, const void* k,
+cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, const void* k,
                                   const void* v, int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim,
                                   float scale, void* out, int32_t* err, cudaStream_t s);
 

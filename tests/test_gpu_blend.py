@@ -126,3 +126,32 @@ def test_full_size_workloads(cb, name, layers):
     o = oracle_layers(cfg, layers, attention_rows=pick)
     for layer in layers:
         compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])))
+
+
+@pytest.mark.parametrize("name,layers", [("mistral7b", 4), ("tiny", 1)])
+def test_request_scheduling_matches_layer_by_layer(cb, name, layers):
+    # cb_blend_request overlaps layers on several streams; its outputs must be the same bytes
+    # as calling cb_blend_layer layer after layer.
+    cfg = get_config(name)
+    plan = cb.Plan.from_config(cfg)
+    sets = hkvd_noise_sets(cfg)
+    ins = [layer_tensors(generate_layer(cfg, layer, sets)) for layer in range(1, layers + 1)]
+    seq = [cb.LayerBuffers(plan) for _ in range(layers)]
+    req = [cb.LayerBuffers(plan) for _ in range(layers)]
+    cand = None
+    for li in range(layers):
+        cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=seq[li], **ins[li])
+        cand = seq[li].sel_tok
+    for _ in range(2):  # twice: the second call reuses the plan's streams and events
+        cb.cb_blend_request(plan, [dict(bufs=req[li], **ins[li]) for li in range(layers)])
+    torch.cuda.synchronize()
+    plan.check()
+    for li in range(layers):
+        _, k, mq, _ = plan.layer_sizes(li + 1)
+        a, b = seq[li], req[li]
+        assert torch.equal(a.sel_tok[:k], b.sel_tok[:k]) and torch.equal(a.sel_row[:k], b.sel_row[:k])
+        for f in ("k_fused", "v_fused"):
+            assert torch.equal(getattr(a, f).view(torch.int16), getattr(b, f).view(torch.int16))
+        for f in ("q_rot", "out"):
+            assert torch.equal(getattr(a, f)[:mq].view(torch.int16), getattr(b, f)[:mq].view(torch.int16))
+    plan.close()
