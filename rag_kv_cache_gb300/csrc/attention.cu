@@ -440,17 +440,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool masking = __any_sync(0xffffffffu, lim < kBN - 1);
       const uint32_t s_addr = lane_base + col_s(wg);
 
-      // Rescale O and l to a new reference (O holds this warpgroup's sum through its previous
+      // Rescale l and O to a new reference (O holds this warpgroup's sum through its previous
       // tile; that PV is complete because S_j was issued after it).
       auto rescale_to = [&](float m_new, bool want) -> bool {
-        const bool w2 = mbar_wait(obar, (it - 1) & 1, abort_flag, p.err, 22 + wg);
-        if (!__all_sync(0xffffffffu, w2)) return false;
-        tc_fence_after();
         const float alpha = want ? ex2(m_ref - m_new) : 1.0f;
         if (want) {
           l *= alpha;
           m_ref = m_new;
         }
+        if (it == 0) return true;  // no P V into O yet: nothing else to scale
+        const bool w2 = mbar_wait(obar, (it - 1) & 1, abort_flag, p.err, 22 + wg);
+        if (!__all_sync(0xffffffffu, w2)) return false;
+        tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -463,31 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
-      if (it == 0) {
-        // First tile of this warpgroup: take the row max as the reference (a max-only pass).
-        float pm[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) pm[q] = -INFINITY;
-        {
-          uint32_t ca[32], cb[32];
-          tmem_ld_x32_async(s_addr, ca);
-          tmem_wait_ld(ca);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
-            uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
-            if (ch < 3) tmem_ld_x32_async(s_addr + (ch + 1) * 32, nxt);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(cur[c]);
-              pm[c & 7] = fmaxf(pm[c & 7], v);
-            }
-            if (ch < 3) tmem_wait_ld(nxt);
-          }
-        }
-        m_ref = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                      fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
-      } else {
+      if (it > 0) {
         // Lazy rescale: move the reference up only once the max has grown by more than 2^8.
         const bool want = m_seen > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, want) && !rescale_to(m_seen, want)) {
@@ -496,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       {
-        // One pass against the current reference. Each 32-key chunk is checked before its
-        // exponentials: every exponent at most kOverflowGuard keeps P and the fp32 sums finite.
+        // One pass against the current reference (0 for a row that has none yet). Each 32-key
+        // chunk is checked before its P is stored: every exponent at most kOverflowGuard keeps P
+        // and the fp32 sums finite.
         // P chunk ch (keys 32ch..) is stored in columns 16ch..16ch+15, which hold keys already read.
         float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;  // reference 0 while nothing was visible
         float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -535,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tm[e & 3] = fmaxf(tm[e & 3], fmaxf(t0, t1));
               }
               const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
-              if (__any_sync(0xffffffffu, tmax > kOverflowGuard)) {
+              // Guard: no exponent above 2^64, and while a row has no reference yet (first tile,
+              // reference 0) none of its maxima below 2^-64 either (its P would underflow).
+              const bool risky =
+                  tmax > kOverflowGuard || (m_ref == -INFINITY && tmax < -kOverflowGuard && tmax > -INFINITY);
+              if (__any_sync(0xffffffffu, risky)) {
                 bail = ch;  // nothing of this chunk was stored: its S columns are intact
               } else {
                 pm[ch] = tmax;

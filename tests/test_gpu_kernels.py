@@ -289,3 +289,29 @@ def test_attention_score_jumps_past_the_overflow_guard(cb):
     got = bf16_bits_to_f64(bf16_bits(out))
     assert np.all(np.isfinite(got))
     assert_close_bf16(got, ref, what="attention with score jumps")
+
+
+def test_attention_first_tile_scores_far_below_zero(cb):
+    # The first key tile of each softmax warpgroup is processed against reference 0; rows whose
+    # scores there lie far below 0 (P would underflow) must take the guarded path and stay exact.
+    hq, hkv, d, n_keys = 8, 2, 128, 600
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=n_keys - 1, n_suffix=1)
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(31)
+    q_pos = np.sort(np.concatenate([rng.choice(np.arange(0, 128), 30, replace=False),
+                                    rng.choice(np.arange(128, 256), 30, replace=False),
+                                    rng.choice(np.arange(256, n_keys), 30, replace=False)]))
+    mq = q_pos.size
+    q = f32_to_bf16_bits((-1.0 - 0.05 * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    kf = rng.standard_normal((n_keys, hkv, d)).astype(np.float32)
+    kf[:256] = 5.0 + 0.1 * kf[:256]  # tiles 0 and 1: scores near -640 (raw), far below 0
+    k = f32_to_bf16_bits(kf)
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    got = bf16_bits_to_f64(bf16_bits(out))
+    assert np.all(np.isfinite(got))
+    assert_close_bf16(got, ref, what="attention with very negative first-tile scores")
