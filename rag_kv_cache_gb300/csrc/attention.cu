@@ -11,21 +11,28 @@
 // so every K/V tile it loads serves all G heads. Key tiles are 128 keys; the
 // CTA visits key tiles 0 .. (largest query position in the tile) / 128.
 //
-// Roles (352 threads):
+// Roles (384 threads):
 //   WG0, WG1 (warps 0-7) softmax: thread r of each owns query row r (TMEM lane
-//              r); WG0 takes the even key tiles, WG1 the odd ones, each with its
+//              r); WG h takes keys [64h, 64h + 64) of every key tile, with its
 //              own running max / sum and its own O accumulator, so the two
-//              softmaxes overlap each other and the tensor core; the two partial
-//              results are merged in the epilogue.
+//              halves of a tile are exponentiated at the same time; the two
+//              partial results are merged in the epilogue.
 //   warp 8     TMA producer of Q (once) and of K tiles (3-stage ring; a stage
 //              is refilled as soon as its S = Q K^T is done);
-//   warp 9     MMA issuer (tcgen05.mma, bf16 in, fp32 accumulate);
-//   warp 10    TMA producer of V tiles (2-stage ring, refilled after P V).
-// TMEM columns: S buffers [0,128) and [128,256) (tile j uses buffer j % 2),
-// O accumulators [256, 256+D) and [256+D, 256+2D). P (bf16) overwrites the first
-// 64 columns of its S buffer and is the A operand of the PV MMA from TMEM.
-// A softmax thread reads its S row from TMEM in 32-column chunks, the next
-// chunk's load in flight while the current one is processed.
+//   warp 9     issuer of S = Q K^T (tcgen05.mma, bf16 in, fp32 accumulate);
+//   warp 10    TMA producer of V tiles (2-stage ring, refilled after P V);
+//   warp 11    issuer of O += P V.
+// TMEM columns: S [0,128) (one N = 128 MMA chain per key tile; WG h reads
+// columns [64h, 64h + 64)); P (bf16 pairs) in [128, 256), buffer b = tile % 2 of
+// WG h at 128 + 64b + 32h; O accumulators [256, 256+D) and [256+D, 256+2D).
+// The softmax copies its 64 scores to registers and hands S back at once, so
+// S_{j+1} = Q K_{j+1}^T runs on the tensor core while tile j is exponentiated;
+// P V_j, the two halves into their own O, runs as soon as both halves of P_j are
+// in TMEM. S and P V come from two issuing threads, each sleeping on its own
+// inputs, so the two streams interleave on the tensor core without one waiting
+// behind the other; operand descriptors are formed once and advanced by
+// compile-time offsets (building them per instruction made the issue, not the
+// tensor core, the bottleneck).
 //
 // Every mbarrier wait is bounded (2 s by the global timer). A wait that gives
 // up records a timeout in the error word, raises a CTA-wide abort flag that
@@ -42,21 +49,25 @@ namespace cb {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBN = 128;     // keys per tile
+constexpr int kHalf = kBN / 2;  // keys of a tile per softmax warpgroup
 constexpr int kKStages = 3;  // depth of the K ring
 constexpr int kVStages = 2;  // depth of the V ring (Q + 3 K + 2 V tiles = 192 KiB for D = 128)
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;  // per softmax warpgroup
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpProducerV = 10;
+constexpr int kWarpMmaPv = 11;
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t col_o(int b, int d) { return 256u + (uint32_t)(b * d); }
+// TMEM columns: S (fp32) [0,128), warpgroup h's half at 64h; P (bf16 pairs) of warpgroup h in
+// buffer b at 128 + 64b + 32h; O accumulators [256, 256 + D) and [256 + D, 256 + 2D).
+__host__ __device__ constexpr uint32_t col_s(int h) { return (uint32_t)(h * kHalf); }
+__host__ __device__ constexpr uint32_t col_p(int h, int b) { return 128u + (uint32_t)(b * 64 + h * 32); }
+__host__ __device__ constexpr uint32_t col_o(int h, int d) { return 256u + (uint32_t)(h * d); }
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr uint32_t kSuspendHintNs = 200000;  // a sleeping waiter re-checks abort and time at least this often
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
-constexpr float kOverflowGuard = 64.0f;    // log2 units: largest exponent the one-pass softmax accepts
 
 struct Bars {
   uint64_t q_full;
@@ -64,9 +75,10 @@ struct Bars {
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t s_full;      // S_j in TMEM (MMA commit)
+  uint64_t s_free;      // S_j copied to registers by all eight softmax warps
+  uint64_t p_full[2];   // P_j (both halves) in TMEM buffer j % 2 (eight softmax warps)
+  uint64_t pv_done[2];  // P_j V_j accumulated into both O (MMA commit), buffer j % 2 free again
   uint64_t drain;
 };
 
@@ -151,6 +163,44 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
       }
     }
   }
+}
+
+// Non-blocking test: true once the phase of parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Busy-wait for the waits on the tile loop's critical path: a thread suspended in try_wait
+// resumes several hundred cycles after the phase completes, a polling one within tens.
+// Same limit and abort behaviour as mbar_wait.
+__device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                            int site) {
+  const uint64_t t0 = global_timer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test(bar, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        record_error(err, kErrTimeout, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          int site) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_spin_slow(bar, parity, abort_flag, err, site);
 }
 
 // Wait for the phase of parity `parity` to complete; false on abort or timeout.
@@ -258,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kQBytes = kBM * D * 2;
   constexpr uint32_t kKVBytes = kBN * D * 2;
   constexpr uint32_t kQBox = kBM * 128;   // bytes of one 64-column box of Q
-  constexpr uint32_t kKVBox = kBN * 128;  // bytes of one 64-column box of K or V
+  constexpr uint32_t kKVBox = kBN * 128;  // bytes of one 64-column box of a K or V tile
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -267,12 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_maxpos;
   __shared__ float s_ml[2][2][kBM];  // [warpgroup][max, sum][row]
 
+  pdl_launch_dependents();
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base;
   const uint32_t sK0 = base + kQBytes;
   const uint32_t sV0 = sK0 + kKStages * kKVBytes;
 
-  pdl_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int lin = blockIdx.x;
   const int tile = p.n_qtiles - 1 - lin / p.hkv;  // later (longer) query tiles first
@@ -290,12 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.s_free), 2 * kSoftmaxThreads / 32);  // one arrival per softmax warp
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars.s_full[b]), 1);
-      mbar_init(smem_u32(&bars.p_full[b]), kSoftmaxThreads / 32);  // one arrival per softmax warp
+      mbar_init(smem_u32(&bars.p_full[b]), 2 * kSoftmaxThreads / 32);
       mbar_init(smem_u32(&bars.pv_done[b]), 1);
     }
-    mbar_init(smem_u32(&bars.drain), 1);
+    mbar_init(smem_u32(&bars.drain), 2);  // one commit from each issuing thread
     s_abort = 0;
     s_maxpos = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -308,9 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   __syncthreads();
-  // The query rows, positions and fused K/V come from the kernels before this one on the stream,
-  // unless the caller orders them by other means (events) and lets this kernel overlap its
-  // same-stream predecessor.
+  // The query rows, positions and fused K/V come from the kernels before this one on the stream.
   if (p.wait_prior) pdl_wait();
 
   // Query position of each softmax thread's row; padded rows repeat the tile's last token.
@@ -377,40 +426,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = nv - kVStages < 0 ? 0 : nv - kVStages; j < nv; ++j)
         mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
-    } else if (warp == kWarpMma && lane == 0) {
+    } else if ((warp == kWarpMma || warp == kWarpMmaPv) && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t idesc_o = idesc_bf16(kBM, D, true);
-      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, p.err, 10);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kKStages, b = j & 1;
-        if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / kKStages) & 1, abort_flag, p.err, 11)) return false;
-        tc_fence_after();
+      // Operand descriptors are formed once; each MMA adds a compile-time offset to the start
+      // address field (shared addresses stay below 256 KiB, so the 14-bit field never carries).
+      bool ok = true;
+      if (warp == kWarpMma) {
+        // S_j = Q K_j^T once S_{j-1} has been copied out of TMEM by all softmax warps.
+        const uint64_t dq = sdesc(sQ, 16, 1024);
+        const uint64_t dk0 = sdesc(sK0, 16, 1024);
+        ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, p.err, 10);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int st = j % kKStages;
+          if (j > 0 && !mbar_spin(smem_u32(&bars.s_free), (j - 1) & 1, abort_flag, p.err, 15)) break;
+          if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / kKStages) & 1, abort_flag, p.err, 11)) break;
+          tc_fence_after();
+          const uint64_t dk = dk0 + (uint64_t)((st * kKVBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int bx = ks / 4, kk = ks % 4;
-          const uint64_t a = sdesc(sQ + bx * kQBox + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc(sK0 + st * kKVBytes + bx * kKVBox + kk * 32, 16, 1024);
-          mma_ss(tmem + col_s(b), a, bd, idesc_s, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int bx = ks / 4, kk = ks % 4;
+            mma_ss(tmem, dq + (uint64_t)((bx * kQBox + kk * 32) >> 4), dk + (uint64_t)((bx * kKVBox + kk * 32) >> 4),
+                   idesc_s, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&bars.k_empty[st]));
+          tc_commit(smem_u32(&bars.s_full));
         }
-        tc_commit(smem_u32(&bars.k_empty[st]));
-        tc_commit(smem_u32(&bars.s_full[b]));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_kv > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int b = j & 1, st = j % kVStages;
-        if (!mbar_wait(smem_u32(&bars.p_full[b]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
-        if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / kVStages) & 1, abort_flag, p.err, 13)) break;
-        tc_fence_after();
+      } else {
+        // O_h += P_{j,h} V_{j,h} for both halves h once both halves of P_j are in TMEM.
+        const uint64_t dv0 = sdesc(sV0, kKVBox, 1024);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int b = j & 1, st = j % kVStages;
+          if (!mbar_spin(smem_u32(&bars.p_full[b]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
+          if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / kVStages) & 1, abort_flag, p.err, 13)) break;
+          tc_fence_after();
+          const uint64_t dv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = sdesc(sV0 + st * kKVBytes + ks * 16 * 128, kKVBox, 1024);
-          mma_ts(tmem + col_o(b, D), tmem + col_s(b) + ks * 8, bd, idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int ks = 0; ks < kHalf / 16; ++ks)
+              mma_ts(tmem + col_o(h, D), tmem + col_p(h, b) + ks * 8,
+                     dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
+          }
+          tc_commit(smem_u32(&bars.v_empty[st]));
+          tc_commit(smem_u32(&bars.pv_done[b]));
         }
-        tc_commit(smem_u32(&bars.v_empty[st]));
-        tc_commit(smem_u32(&bars.pv_done[b]));
-        if (j + 2 < n_kv && !issue_s(j + 2)) break;
       }
       // All tensor-core work issued by this CTA completes before TMEM is freed.
       tc_commit(smem_u32(&bars.drain));
@@ -418,193 +479,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int wg = warp / 4;  // 0: even key tiles, 1: odd key tiles
+    const int wg = warp / 4;  // this warpgroup takes keys [64 wg, 64 wg + 64) of every key tile
     const int r = threadIdx.x % kBM;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-    const uint32_t sbar = smem_u32(&bars.s_full[wg]);
-    const uint32_t pbar = smem_u32(&bars.p_full[wg]);
-    const uint32_t obar = smem_u32(&bars.pv_done[wg]);
-    // m_ref: reference max (log2 units) that this warpgroup's O and l are scaled to;
-    // m_seen: the largest row max seen so far (m_ref catches up lazily).
-    float m_ref = -INFINITY, m_seen = -INFINITY, l = 0.0f;
+    const uint32_t sbar = smem_u32(&bars.s_full);
+    const uint32_t fbar = smem_u32(&bars.s_free);
+    // m_ref: reference max (log2 units) that this warpgroup's O and l are scaled to.
+    float m_ref = -INFINITY, l = 0.0f;
     bool ok = true;
-    int it = 0;
-    for (int j = wg; j < n_kv; j += 2, ++it) {
-      const bool w = mbar_wait(sbar, it & 1, abort_flag, p.err, 20 + wg);
+    // Wait until P V_j is complete (barrier pv_done[j % 2], its phase j / 2).
+    auto wait_pv = [&](int j, int site) -> bool {
+      const bool w = mbar_wait(smem_u32(&bars.pv_done[j & 1]), (j >> 1) & 1, abort_flag, p.err, site);
+      return __all_sync(0xffffffffu, w);
+    };
+    for (int j = 0; j < n_kv; ++j) {
+      const bool w = mbar_spin(sbar, j & 1, abort_flag, p.err, 20 + wg);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int lim = my_pos - j * kBN;  // columns c <= lim are visible to this row
-      const bool masking = __any_sync(0xffffffffu, lim < kBN - 1);
-      const uint32_t s_addr = lane_base + col_s(wg);
-
-      // Rescale l and O to a new reference (O holds this warpgroup's sum through its previous
-      // tile; that PV is complete because S_j was issued after it).
-      auto rescale_to = [&](float m_new, bool want) -> bool {
-        const float alpha = want ? ex2(m_ref - m_new) : 1.0f;
-        if (want) {
-          l *= alpha;
-          m_ref = m_new;
-        }
-        if (it == 0) return true;  // no P V into O yet: nothing else to scale
-        const bool w2 = mbar_wait(obar, (it - 1) & 1, abort_flag, p.err, 22 + wg);
-        if (!__all_sync(0xffffffffu, w2)) return false;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(lane_base + col_o(wg, D) + c0, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_x32(lane_base + col_o(wg, D) + c0, o);
-        }
-        tmem_st_wait();
-        return true;
-      };
-
-      if (it > 0) {
-        // Lazy rescale: move the reference up only once the max has grown by more than 2^8.
-        const bool want = m_seen > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, want) && !rescale_to(m_seen, want)) {
-          ok = false;
-          break;
-        }
-      }
+      // Copy this half's 64 scores to registers and hand S back at once: the MMA warp issues
+      // S_{j+1} into it while this tile is exponentiated.
+      uint32_t sv[kHalf];
       {
-        // One pass against the current reference (0 for a row that has none yet). Each 32-key
-        // chunk is checked before its P is stored: every exponent at most kOverflowGuard keeps P
-        // and the fp32 sums finite.
-        // P chunk ch (keys 32ch..) is stored in columns 16ch..16ch+15, which hold keys already read.
-        float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;  // reference 0 while nothing was visible
-        float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        uint64_t ps2[4];  // partial row sums, packed pairs
+        uint32_t(&sa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t(&sb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tmem_ld_x32_async(lane_base + col_s(wg), sa);
+        tmem_ld_x32_async(lane_base + col_s(wg) + 32, sb);
+        tmem_wait_ld(sa);
+        tmem_wait_ld(sb);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fbar);
+      const int lim = my_pos - (j * kBN + wg * kHalf);  // columns c <= lim are visible to this row
+      if (__any_sync(0xffffffffu, lim < kHalf - 1)) {  // diagonal tiles only
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
-        int bail = 4;  // first chunk that failed the guard
-        {
-          uint32_t ca[32], cb[32];
-          tmem_ld_x32_async(s_addr, ca);
-          tmem_wait_ld(ca);
+        for (int c = 0; c < kHalf; ++c)
+          if (c > lim) sv[c] = 0xff800000u;  // -inf
+      }
+
+      // Row max of this half tile from the registers, before any exponential: the reference m_ref
+      // (log2 units) that O and l are scaled to moves up only when a tile's max passes it by more
+      // than 2^8, so every exponent below is at most kRescaleThreshold and O is rescaled rarely.
+      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
-            uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
-            if (ch < 3) tmem_ld_x32_async(s_addr + (ch + 1) * 32, nxt);
-            if (bail == 4) {  // warp-uniform
-              if (masking) {  // diagonal tiles only: hide the keys past this row's position
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                  if (ch * 32 + c > lim) cur[c] = 0xff800000u;  // -inf
-              }
-              // Exponent arguments t = s * scale - m and their exponentials first; the guard on
-              // max t is voted while the exponentials are in flight, and P is stored only if it holds.
-              const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
-              float pv[32];
-              float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float t0, t1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sc2, nm2),
-                          t0, t1);
-                pv[2 * e] = ex2(t0);
-                pv[2 * e + 1] = ex2(t1);
-                tm[e & 3] = fmaxf(tm[e & 3], fmaxf(t0, t1));
-              }
-              const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
-              // Guard: no exponent above 2^64, and while a row has no reference yet (first tile,
-              // reference 0) none of its maxima below 2^-64 either (its P would underflow).
-              const bool risky =
-                  tmax > kOverflowGuard || (m_ref == -INFINITY && tmax < -kOverflowGuard && tmax > -INFINITY);
-              if (__any_sync(0xffffffffu, risky)) {
-                bail = ch;  // nothing of this chunk was stored: its S columns are intact
-              } else {
-                pm[ch] = tmax;
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(pv[2 * e], pv[2 * e + 1]));
-                  pk[e] = pack2(pv[2 * e], pv[2 * e + 1]);
-                }
-                tmem_st_x16(s_addr + ch * 16, pk);
-              }
-            }
-            if (ch < 3) tmem_wait_ld(nxt);
-          }
+      for (int c = 0; c < kHalf; ++c) tm[c & 3] = fmaxf(tm[c & 3], __uint_as_float(sv[c]));
+      const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
+      const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
+      if (__any_sync(0xffffffffu, up)) {
+        // alpha = 2^(m_ref - mt): 0 for a row that had nothing visible (its O and l are zero).
+        const float alpha = up ? ex2(m_ref - mt) : 1.0f;
+        const bool scale_o = up && m_ref != -INFINITY;
+        if (up) {
+          l *= alpha;
+          m_ref = mt;
         }
-        // row max of the scaled scores seen in this tile (pm holds max t = s * scale - m)
-        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) - neg_m;
-        if (bail < 4) {
-          // Rare: a row's max jumped past the guard at chunk `bail`. Chunks bail.. are intact in
-          // TMEM; find the tile's max, move O, l, the partial sums and the P chunks already
-          // stored to it, then finish the tile against it.
-          float rm = -INFINITY;
-#pragma unroll 1
-          for (int ch = bail; ch < 4; ++ch) {
-            uint32_t c32[32];
-            tmem_ld_x32(s_addr + ch * 32, c32);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float v = (masking && ch * 32 + c > lim) ? -INFINITY : __uint_as_float(c32[c]);
-              rm = fmaxf(rm, v);
-            }
-          }
-          mx = fmaxf(mx, rm * p.scale_log2);
-          // The reference never moves down; rows with nothing visible yet keep all-zero values.
-          const float m_eff = -neg_m;  // reference of this tile's P chunks and sums so far
-          const float m_new = fmaxf(m_ref, mx);
-          const float beta = m_new == -INFINITY ? 1.0f : ex2(fminf(m_eff - m_new, 126.0f));
-          if (!rescale_to(m_new, m_new > m_ref)) {
+        // O holds this warpgroup's sum through tile j - 1: wait for that P V, then scale it.
+        if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
+          if (!wait_pv(j - 1, 22 + wg)) {
             ok = false;
             break;
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) ps2[q] = f2_fma(ps2[q], f2_pack(beta, beta), f2_pack(0.0f, 0.0f));
+          tc_fence_after();
+          const float a = scale_o ? alpha : 1.0f;
 #pragma unroll 1
-          for (int ch = 0; ch < bail; ++ch) {
-            uint32_t q16[16];
-            tmem_ld_x16(s_addr + ch * 16, q16);
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(lane_base + col_o(wg, D) + c0, o);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              q16[e] = pack2(__uint_as_float(q16[e] << 16) * beta, __uint_as_float(q16[e] & 0xffff0000u) * beta);
-            tmem_st_x16(s_addr + ch * 16, q16);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st_x32(lane_base + col_o(wg, D) + c0, o);
           }
-          neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
-#pragma unroll 1
-          for (int ch = bail; ch < 4; ++ch) {
-            uint32_t c32[32];
-            tmem_ld_x32(s_addr + ch * 32, c32);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float v0 = (masking && ch * 32 + 2 * e > lim) ? -INFINITY : __uint_as_float(c32[2 * e]);
-              const float v1 = (masking && ch * 32 + 2 * e + 1 > lim) ? -INFINITY : __uint_as_float(c32[2 * e + 1]);
-              const float p0 = ex2(fmaf(v0, p.scale_log2, neg_m));
-              const float p1 = ex2(fmaf(v1, p.scale_log2, neg_m));
-              ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
-              pk[e] = pack2(p0, p1);
-            }
-            tmem_st_x16(s_addr + ch * 16, pk);
-          }
-        } else if (m_ref == -INFINITY && mx > -INFINITY) {
-          m_ref = 0.0f;  // this pass used reference 0
+          tmem_st_wait();
         }
-        float sa, sb;
-        f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa, sb);
-        l += sa + sb;
-        m_seen = fmaxf(m_seen, mx);
       }
+      // P = 2^(s * scale - m_ref) <= 2^8, packed to bf16, and its row sum. A row with nothing visible
+      // yet has only -inf scores, so P = 0 (the offset 0 stands in for its missing reference).
+      uint32_t pk[kHalf / 2];
+      {
+        const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
+        uint64_t ps2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
+#pragma unroll
+        for (int e = 0; e < kHalf / 2; ++e) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2, nm2), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
+          pk[e] = pack2(p0, p1);
+        }
+        float sa_, sb_;
+        f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa_, sb_);
+        l += sa_ + sb_;
+      }
+      // P buffer j % 2 was last read by P V_{j-2}.
+      if (j >= 2 && !wait_pv(j - 2, 24 + wg)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_x32(lane_base + col_p(wg, j & 1), pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pbar);
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[j & 1]));
     }
-    const int n_mine = (n_kv - wg + 1) / 2;
-    if (ok && n_mine > 0) {
-      const bool w = mbar_wait(obar, (n_mine - 1) & 1, abort_flag, p.err, 24 + wg);
-      ok = __all_sync(0xffffffffu, w);
-    }
+    if (ok) ok = wait_pv(n_kv - 1, 26 + wg);
     // Merge the two warpgroups' partial results; each writes half of the columns.
     s_ml[wg][0][r] = m_ref;
     s_ml[wg][1][r] = l;
@@ -618,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float a0 = m0 == -INFINITY ? 0.0f : ex2(m0 - mm);
       const float a1 = m1 == -INFINITY ? 0.0f : ex2(m1 - mm);
       const float inv = 1.0f / (s_ml[0][1][r] * a0 + s_ml[1][1][r] * a1);
-      const bool have1 = n_kv > 1;
       const int t = t0 + r / p.group;
       const bool valid = t <= t_last;
       uint8_t* dst = p.out + ((size_t)t * p.hq + (size_t)g * p.group + (r % p.group)) * D * 2;
@@ -626,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
         uint32_t o0[32], o1[32];
         tmem_ld_x32(lane_base + col_o(0, D) + c0, o0);
-        if (have1) tmem_ld_x32(lane_base + col_o(1, D) + c0, o1);
+        tmem_ld_x32(lane_base + col_o(1, D) + c0, o1);
         if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -634,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float v0 = __uint_as_float(o0[q * 8 + e]) * a0;
-              const float v1 = have1 ? __uint_as_float(o1[q * 8 + e]) * a1 : 0.0f;
+              const float v1 = __uint_as_float(o1[q * 8 + e]) * a1;
               f[e] = (v0 + v1) * inv;
             }
             *reinterpret_cast<uint4*>(dst + (c0 + q * 8) * 2) = pack8(f);
@@ -688,7 +671,7 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   const cuuint32_t qb[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)tq};
   const cuuint64_t kd[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)n_keys};
   const cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
-  const cuuint32_t kbx[3] = {64, 1, (cuuint32_t)kBN};
+  const cuuint32_t kbx[3] = {64, 1, (cuuint32_t)kBN};  // a K or V tile: kBN keys of one kv head
   if (!encode_map(&tq_map, q, 4, qd, qs, qb) || !encode_map(&tk_map, k, 3, kd, ks, kbx) ||
       !encode_map(&tv_map, v, 3, kd, ks, kbx))
     return cudaErrorInvalidValue;

@@ -262,10 +262,10 @@ def test_attention_peaked_scores_force_rescale(cb):
     assert_close_bf16(got, ref, what="peaked attention")
 
 
-def test_attention_score_jumps_past_the_overflow_guard(cb):
+def test_attention_score_jumps_between_key_tiles(cb):
     # Keys whose scores exceed everything earlier by far more than 2^64 (in base-2 units of the
-    # scaled score), in tiles handled by both softmax warpgroups: the one-pass softmax must move
-    # its reference (and the P values it already stored) instead of overflowing.
+    # scaled score), in both halves of the key tiles: the softmax must move its reference and
+    # rescale what it accumulated instead of overflowing.
     hq, hkv, d, n_keys = 8, 2, 128, 1000
     cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
                               chunk_len=n_keys - 1, n_suffix=1)
@@ -292,8 +292,8 @@ def test_attention_score_jumps_past_the_overflow_guard(cb):
 
 
 def test_attention_first_tile_scores_far_below_zero(cb):
-    # The first key tile of each softmax warpgroup is processed against reference 0; rows whose
-    # scores there lie far below 0 (P would underflow) must take the guarded path and stay exact.
+    # Rows whose scores in the first key tiles lie far below 0 (2^score would underflow fp32): the
+    # softmax reference must follow the row max, not start from 0.
     hq, hkv, d, n_keys = 8, 2, 128, 600
     cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
                               chunk_len=n_keys - 1, n_suffix=1)
