@@ -19,20 +19,27 @@
 //              partial results are merged in the epilogue.
 //   warp 8     TMA producer of Q (once) and of K tiles (3-stage ring; a stage
 //              is refilled as soon as its S = Q K^T is done);
-//   warp 9     issuer of S = Q K^T (tcgen05.mma, bf16 in, fp32 accumulate);
-//   warp 10    TMA producer of V tiles (2-stage ring, refilled after P V);
-//   warp 11    issuer of O += P V.
-// TMEM columns: S [0,128) (one N = 128 MMA chain per key tile; WG h reads
-// columns [64h, 64h + 64)); P (bf16 pairs) in [128, 256), buffer b = tile % 2 of
-// WG h at 128 + 64b + 32h; O accumulators [256, 256+D) and [256+D, 256+2D).
-// The softmax copies its 64 scores to registers and hands S back at once, so
-// S_{j+1} = Q K_{j+1}^T runs on the tensor core while tile j is exponentiated;
-// P V_j, the two halves into their own O, runs as soon as both halves of P_j are
-// in TMEM. S and P V come from two issuing threads, each sleeping on its own
-// inputs, so the two streams interleave on the tensor core without one waiting
-// behind the other; operand descriptors are formed once and advanced by
-// compile-time offsets (building them per instruction made the issue, not the
-// tensor core, the bottleneck).
+//   warp 9     issuer of both products (tcgen05.mma, bf16 in, fp32 accumulate);
+//   warp 10    TMA producer of V tiles (3-stage ring, refilled after P V);
+//   warp 11    the issuer's waiter: it polls the barriers a round of MMAs depends
+//              on and meets the issuer on a named barrier (bar.red.and carries
+//              whether the inputs are ready). A warp that has just
+//              issued MMAs waits 100-200 cycles on its next shared-memory access
+//              (an mbarrier test included) while a named barrier returns at once,
+//              so the issuer itself never touches an mbarrier in the tile loop.
+// TMEM columns: S in two buffers, tile j in buffer j % 2 at 128 (j % 2) (one
+// N = 128 MMA chain per key tile; WG h reads its 64 columns); each warpgroup
+// writes its P_j (bf16 pairs, 32 columns) over the first half of its own S_j
+// columns once it has copied them out; O accumulators at 256 and 256 + D.
+// One thread issues every MMA, and tcgen05.mma operations from one thread run
+// in issue order: S_{j+2} is issued into buffer j % 2 right after P V_j, which
+// reads P_j from it, with no completion wait in between, so the tensor core
+// always has the next scores queued behind the current P V while the softmax
+// works on tile j + 1. The softmax never hands a buffer back: S_j is consumed
+// before P_j is written, and P_j before S_{j+2} overwrites it, by construction.
+// The issuing warp runs converged and one elected lane issues, so the loop
+// index, stages and operand descriptors are warp-uniform values in uniform
+// registers; descriptors are formed once and advanced by compile-time offsets.
 //
 // Every mbarrier wait is bounded (2 s by the global timer). A wait that gives
 // up records a timeout in the error word, raises a CTA-wide abort flag that
@@ -52,18 +59,20 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;     // keys per tile
 constexpr int kHalf = kBN / 2;  // keys of a tile per softmax warpgroup
 constexpr int kKStages = 3;  // depth of the K ring
-constexpr int kVStages = 2;  // depth of the V ring (Q + 3 K + 2 V tiles = 192 KiB for D = 128)
+constexpr int kVStages = 3;  // depth of the V ring (Q + 3 K + 3 V tiles = 224 KiB for D = 128): a V
+                             // stage is refilled only after its P V completes, so a load has two
+                             // tiles of lead before its P V
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;  // per softmax warpgroup
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpProducerV = 10;
-constexpr int kWarpMmaPv = 11;
+constexpr int kWarpWaiter = 11;
+constexpr int kBarIssue = 2;  // named barrier: issuer + waiter (64 threads)
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S (fp32) [0,128), warpgroup h's half at 64h; P (bf16 pairs) of warpgroup h in
-// buffer b at 128 + 64b + 32h; O accumulators [256, 256 + D) and [256 + D, 256 + 2D).
-__host__ __device__ constexpr uint32_t col_s(int h) { return (uint32_t)(h * kHalf); }
-__host__ __device__ constexpr uint32_t col_p(int h, int b) { return 128u + (uint32_t)(b * 64 + h * 32); }
+// TMEM columns: S (fp32) buffer b at 128 b, warpgroup h's half at +64 h (P_j over the first 32
+// columns of that half); O accumulators at 256 + h D.
+__host__ __device__ constexpr uint32_t col_s(int b, int h) { return (uint32_t)(b * kBN + h * kHalf); }
 __host__ __device__ constexpr uint32_t col_o(int h, int d) { return 256u + (uint32_t)(h * d); }
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr uint32_t kSuspendHintNs = 200000;  // a sleeping waiter re-checks abort and time at least this often
@@ -75,10 +84,9 @@ struct Bars {
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full;      // S_j in TMEM (MMA commit)
-  uint64_t s_free;      // S_j copied to registers by all eight softmax warps
-  uint64_t p_full[2];   // P_j (both halves) in TMEM buffer j % 2 (eight softmax warps)
-  uint64_t pv_done[2];  // P_j V_j accumulated into both O (MMA commit), buffer j % 2 free again
+  uint64_t s_full[2];   // S_j in TMEM buffer j % 2 (MMA commit); phase j / 2
+  uint64_t p_full[2];   // P_j (both halves) in TMEM buffer j % 2 (eight softmax warps); phase j / 2
+  uint64_t pv_done[2];  // P_j V_j accumulated into both O (MMA commit); phase j / 2
   uint64_t drain;
 };
 
@@ -148,9 +156,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Slow path of mbar_wait: sleep-wait with a time limit.
+// Slow path of mbar_wait: sleep-wait with a time limit. A few plain try_waits come first: reading
+// %globaltimer takes hundreds of cycles, so the clock for the limit starts only for a long wait.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                             int site, bool honour_abort) {
+  for (int n = 0; n < 16; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
@@ -183,6 +194,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // Same limit and abort behaviour as mbar_wait.
 __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                             int site) {
+  // Poll without the clock first (reading %globaltimer takes hundreds of cycles and would delay
+  // noticing a phase that completes within the first few polls); then with the time limit.
+  for (int n = 0; n < 512; ++n)
+    if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_test(bar, parity)) return true;
@@ -253,6 +268,23 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
       : "memory");
 }
 
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -315,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_maxpos;
-  __shared__ float s_ml[2][2][kBM];  // [warpgroup][max, sum][row]
 
   pdl_launch_dependents();
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -340,13 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_full[s]), 1);
       mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars.s_full), 1);
-    mbar_init(smem_u32(&bars.s_free), 2 * kSoftmaxThreads / 32);  // one arrival per softmax warp
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars.p_full[b]), 2 * kSoftmaxThreads / 32);
+      mbar_init(smem_u32(&bars.s_full[b]), 1);
+      mbar_init(smem_u32(&bars.p_full[b]), 2 * kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(smem_u32(&bars.pv_done[b]), 1);
     }
-    mbar_init(smem_u32(&bars.drain), 2);  // one commit from each issuing thread
+    mbar_init(smem_u32(&bars.drain), 1);
     s_abort = 0;
     s_maxpos = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -426,93 +456,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = nv - kVStages < 0 ? 0 : nv - kVStages; j < nv; ++j)
         mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
-    } else if ((warp == kWarpMma || warp == kWarpMmaPv) && lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
-      constexpr uint32_t idesc_o = idesc_bf16(kBM, D, true);
-      // Operand descriptors are formed once; each MMA adds a compile-time offset to the start
-      // address field (shared addresses stay below 256 KiB, so the 14-bit field never carries).
-      bool ok = true;
-      if (warp == kWarpMma) {
-        // S_j = Q K_j^T once S_{j-1} has been copied out of TMEM by all softmax warps.
+    } else if (warp == kWarpMma || warp == kWarpWaiter) {
+      // Rounds: round -1 issues S_0 and S_1; round j issues P V_j and then S_{j+2} into the same
+      // buffer. The waiter polls the round's barriers (Q and K_0, K_1; then V_j, K_{j+2} and P_j),
+      // publishes whether they completed, and meets the issuer on named barrier kBarIssue; while
+      // the issuer feeds the tensor core round j, the waiter already polls for round j + 1.
+      // Both warps arrive; every thread gets the AND of the predicates (the waiter's "inputs ready").
+      auto rendezvous = [&](bool ok) -> bool {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, %2, 64, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"(ok ? 1u : 0u), "n"(kBarIssue)
+            : "memory");
+        return r != 0;
+      };
+      const int n_rounds = n_kv + 1;
+      if (warp == kWarpWaiter) {
+        auto spin_all = [&](uint32_t bar, uint32_t parity, int site) -> bool {
+          return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site));
+        };
+        auto k_ready = [&](int j) {
+          return spin_all(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, 11);
+        };
+        for (int rd = -1; rd + 1 < n_rounds; ++rd) {
+          bool ok;
+          if (rd < 0) {
+            ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0) && (n_kv < 2 || k_ready(1));
+          } else {
+            const int j = rd;
+            ok = spin_all(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, 13) &&
+                 (j + 2 >= n_kv || k_ready(j + 2)) && spin_all(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, 12);
+          }
+          if (!rendezvous(ok)) break;
+        }
+      } else {
+        constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
+        constexpr uint32_t idesc_o = idesc_bf16(kBM, D, true);
         const uint64_t dq = sdesc(sQ, 16, 1024);
         const uint64_t dk0 = sdesc(sK0, 16, 1024);
-        ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, p.err, 10);
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int st = j % kKStages;
-          if (j > 0 && !mbar_spin(smem_u32(&bars.s_free), (j - 1) & 1, abort_flag, p.err, 15)) break;
-          if (!mbar_wait(smem_u32(&bars.k_full[st]), (j / kKStages) & 1, abort_flag, p.err, 11)) break;
-          tc_fence_after();
+        const uint64_t dv0 = sdesc(sV0, kKVBox, 1024);
+        // S_j = Q K_j^T into buffer j % 2; elected lane only.
+        auto issue_s = [&](int j) {
+          const int st = j % kKStages, b = j & 1;
           const uint64_t dk = dk0 + (uint64_t)((st * kKVBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const int bx = ks / 4, kk = ks % 4;
-            mma_ss(tmem, dq + (uint64_t)((bx * kQBox + kk * 32) >> 4), dk + (uint64_t)((bx * kKVBox + kk * 32) >> 4),
-                   idesc_s, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + col_s(b, 0), dq + (uint64_t)((bx * kQBox + kk * 32) >> 4),
+                   dk + (uint64_t)((bx * kKVBox + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&bars.k_empty[st]));
-          tc_commit(smem_u32(&bars.s_full));
-        }
-      } else {
-        // O_h += P_{j,h} V_{j,h} for both halves h once both halves of P_j are in TMEM.
-        const uint64_t dv0 = sdesc(sV0, kKVBox, 1024);
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int b = j & 1, st = j % kVStages;
-          if (!mbar_spin(smem_u32(&bars.p_full[b]), (j >> 1) & 1, abort_flag, p.err, 12)) break;
-          if (!mbar_wait(smem_u32(&bars.v_full[st]), (j / kVStages) & 1, abort_flag, p.err, 13)) break;
+          tc_commit(smem_u32(&bars.s_full[b]));
+        };
+        for (int rd = -1; rd + 1 < n_rounds; ++rd) {
+          if (!rendezvous(true)) break;
           tc_fence_after();
-          const uint64_t dv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
+          if (rd < 0) {
+            if (elect_one()) {
+              issue_s(0);
+              if (n_kv > 1) issue_s(1);
+            }
+          } else {
+            // O_h += P_{j,h} V_{j,h} for both halves h, then S_{j+2} into the same buffer
+            // (executed after this P V, which reads P_j from it).
+            const int j = rd, b = j & 1, st = j % kVStages;
+            const uint64_t dv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
+            if (elect_one()) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+              for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int ks = 0; ks < kHalf / 16; ++ks)
-              mma_ts(tmem + col_o(h, D), tmem + col_p(h, b) + ks * 8,
-                     dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
+                for (int ks = 0; ks < kHalf / 16; ++ks)
+                  mma_ts(tmem + col_o(h, D), tmem + col_s(b, h) + ks * 8,
+                         dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
+              }
+              tc_commit(smem_u32(&bars.v_empty[st]));
+              tc_commit(smem_u32(&bars.pv_done[b]));
+              if (j + 2 < n_kv) issue_s(j + 2);
+            }
           }
-          tc_commit(smem_u32(&bars.v_empty[st]));
-          tc_commit(smem_u32(&bars.pv_done[b]));
+          __syncwarp();
         }
+        // All tensor-core work issued by this CTA completes before TMEM is freed.
+        if (elect_one()) tc_commit(smem_u32(&bars.drain));
+        __syncwarp();
+        mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 14, false);
       }
-      // All tensor-core work issued by this CTA completes before TMEM is freed.
-      tc_commit(smem_u32(&bars.drain));
-      mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 14, false);
     }
     __syncwarp();
   } else {
     const int wg = warp / 4;  // this warpgroup takes keys [64 wg, 64 wg + 64) of every key tile
     const int r = threadIdx.x % kBM;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-    const uint32_t sbar = smem_u32(&bars.s_full);
-    const uint32_t fbar = smem_u32(&bars.s_free);
     // m_ref: reference max (log2 units) that this warpgroup's O and l are scaled to.
     float m_ref = -INFINITY, l = 0.0f;
     bool ok = true;
-    // Wait until P V_j is complete (barrier pv_done[j % 2], its phase j / 2).
+    // Wait until P V_j is complete (barrier pv_done[j % 2], its phase j / 2). Polled: a
+    // suspended waiter resumes late, and these waits sit on the tile loop's critical path.
     auto wait_pv = [&](int j, int site) -> bool {
-      const bool w = mbar_wait(smem_u32(&bars.pv_done[j & 1]), (j >> 1) & 1, abort_flag, p.err, site);
+      const bool w = mbar_spin(smem_u32(&bars.pv_done[j & 1]), (j >> 1) & 1, abort_flag, p.err, site);
       return __all_sync(0xffffffffu, w);
     };
     for (int j = 0; j < n_kv; ++j) {
-      const bool w = mbar_spin(sbar, j & 1, abort_flag, p.err, 20 + wg);
+      const int b = j & 1;
+      const bool w = mbar_spin(smem_u32(&bars.s_full[b]), (j >> 1) & 1, abort_flag, p.err, 20 + wg);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // Copy this half's 64 scores to registers and hand S back at once: the MMA warp issues
-      // S_{j+1} into it while this tile is exponentiated.
+      // Copy this half's 64 scores to registers; P_j is later written over their first 32 columns.
       uint32_t sv[kHalf];
       {
         uint32_t(&sa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
         uint32_t(&sb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld_x32_async(lane_base + col_s(wg), sa);
-        tmem_ld_x32_async(lane_base + col_s(wg) + 32, sb);
+        tmem_ld_x32_async(lane_base + col_s(b, wg), sa);
+        tmem_ld_x32_async(lane_base + col_s(b, wg) + 32, sb);
         tmem_wait_ld(sa);
         tmem_wait_ld(sb);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(fbar);
       const int lim = my_pos - (j * kBN + wg * kHalf);  // columns c <= lim are visible to this row
       if (__any_sync(0xffffffffu, lim < kHalf - 1)) {  // diagonal tiles only
 #pragma unroll
@@ -523,9 +589,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Row max of this half tile from the registers, before any exponential: the reference m_ref
       // (log2 units) that O and l are scaled to moves up only when a tile's max passes it by more
       // than 2^8, so every exponent below is at most kRescaleThreshold and O is rescaled rarely.
+      // Four independent chains of three-input max (8 deep each).
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kHalf; ++c) tm[c & 3] = fmaxf(tm[c & 3], __uint_as_float(sv[c]));
+      for (int c = 0; c < kHalf; c += 8) {
+        tm[0] = max3(tm[0], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        tm[1] = max3(tm[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+        tm[2] = max3(tm[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+        tm[3] = max3(tm[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+      }
       const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
       const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
       if (__any_sync(0xffffffffu, up)) {
@@ -576,20 +648,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa_, sb_);
         l += sa_ + sb_;
       }
-      // P buffer j % 2 was last read by P V_{j-2}.
-      if (j >= 2 && !wait_pv(j - 2, 24 + wg)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_x32(lane_base + col_p(wg, j & 1), pk);
+      tmem_st_x32(lane_base + col_s(b, wg), pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[j & 1]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
     }
     if (ok) ok = wait_pv(n_kv - 1, 26 + wg);
     // Merge the two warpgroups' partial results; each writes half of the columns.
+    // [warpgroup][max, sum][row] in the K ring: every K tile has been consumed by now (the last
+    // P V is complete and the S MMAs before it), so the ring is free.
+    float(*s_ml)[2][kBM] = reinterpret_cast<float(*)[2][kBM]>(smem_raw + (sK0 - smem_u32(smem_raw)));
     s_ml[wg][0][r] = m_ref;
     s_ml[wg][1][r] = l;
     tc_fence_before();
@@ -608,8 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
         uint32_t o0[32], o1[32];
-        tmem_ld_x32(lane_base + col_o(0, D) + c0, o0);
-        tmem_ld_x32(lane_base + col_o(1, D) + c0, o1);
+        tmem_ld_x32_async(lane_base + col_o(0, D) + c0, o0);
+        tmem_ld_x32_async(lane_base + col_o(1, D) + c0, o1);
+        tmem_wait_ld(o0);
+        tmem_wait_ld(o1);
         if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
