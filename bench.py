@@ -12,10 +12,11 @@ head_dim 128, r1 = 30% -> r2 = 15%).
 
 Our arm: inputs resident in HBM (per-layer buffers, 1.6 GB per step, larger
 than L2); each step is one cb_blend_request call through the C ABI (all layers,
-pipelined over the plan's streams), replayed as a CUDA graph. A second timed
-region runs the layers one by one with CUDA events between the kernels to give
-each kernel's time (those events serialise the kernels, so that region is
-slower than the headline one).
+pipelined over the plan's streams), replayed as a CUDA graph. Per-kernel times
+come from one more CUDA graph per stage (cb_blend_stage): that stage's kernel
+for every layer that has it, back to back on one stream, replayed `steps`
+times; a kernel's time is the graph's time over its launches (no events
+between kernels, which would serialise their programmatic launch overlap).
 `e2e` repeats the metric through the C ABI from pinned host buffers with the
 host-to-device copies of every layer's inputs and the device-to-host copy of
 its outputs inside the timed region. `cpu_baseline` times the CPU oracle on a
@@ -44,7 +45,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "context tokens blended/s per layer"
 UNIT = "tokens/s"
-STAGES = ("deviation", "topk", "fuse", "query_encode", "attention")
+STAGES = ("deviation", "topk", "fuse", "attention")
 
 
 def parse_args():
@@ -220,12 +221,18 @@ def attention_flops(cfg, sel_tok):
 
 
 def stage_bytes(cfg, n_cand, k, mq, selects):
+    """Algorithmic HBM bytes of one layer's streaming kernels: deviation reads V_new and V_old of
+    the candidates; the fuse pass reads and writes K and V of every row and reads and writes the
+    query rows it encodes."""
     row_kv = cfg.hkv * cfg.head_dim * 2
     row_q = cfg.hq * cfg.head_dim * 2
     return {"deviation": 2.0 * n_cand * row_kv if selects else 0.0,
-            "topk": 8.0 * n_cand if selects else 8.0 * n_cand,
-            "fuse": 4.0 * cfg.n_tokens * row_kv,
-            "query_encode": 2.0 * mq * row_q}
+            "fuse": 4.0 * cfg.n_tokens * row_kv + 2.0 * mq * row_q}
+
+
+def stage_applies(name, size):
+    n_cand, k, mq, selects = size
+    return {"deviation": bool(selects), "topk": bool(selects), "fuse": True, "attention": mq > 0}[name]
 
 
 def traffic_for(kernel_src):
@@ -265,21 +272,13 @@ def run_ours(args, cfg):
     plan = cb.Plan.from_config(cfg)
     bufs = [cb.LayerBuffers(plan, dev) for _ in range(cfg.layers)]
     sizes = [plan.layer_sizes(layer) for layer in range(1, cfg.layers + 1)]
-    # our kernels per layer: deviation + top-k (selecting layers), fuse, query encoding, attention
-    launches_per_step = sum((2 if s[3] else 0) + (3 if s[2] > 0 else 1) for s in sizes)
     stream = torch.cuda.Stream(dev)
 
     layers_spec = [dict(bufs=bufs[li], **d_in[li]) for li in range(cfg.layers)]
 
-    def step(events=None):
-        if events is None:
-            # the whole request in one call: layers pipelined over the plan's streams
-            cb.cb_blend_request(plan, layers_spec, stream=stream)
-            return
-        cand = None
-        for li in range(cfg.layers):  # layer by layer on one stream, with stage events
-            cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=bufs[li], stream=stream, events=events[li], **d_in[li])
-            cand = bufs[li].sel_tok
+    def step():
+        # the whole request in one call: layers pipelined over the plan's streams
+        cb.cb_blend_request(plan, layers_spec, stream=stream)
 
     # warm up eagerly (first launches configure the kernels), check the device error word
     with torch.cuda.stream(stream):
@@ -288,22 +287,9 @@ def run_ours(args, cfg):
     stream.synchronize()
     plan.check()
 
-    n_events = 6
     use_graph = not args.no_graph
     chunk = 32
-    ev_sets = [[[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(cfg.layers)]
-               for _ in range(args.steps)]
-    with torch.cuda.stream(stream):
-        for s in ev_sets:  # create the CUDA events
-            for layer_ev in s:
-                for e in layer_ev:
-                    e.record(stream)
-    stream.synchronize()
-
-    # Two graph sets: the headline timed region replays steps without stage events (events
-    # between kernels would serialise the programmatic launch overlap); the second timed region
-    # replays steps with stage events to time each kernel.
-    plain_graphs, staged_graphs = [], []
+    plain_graphs = []
     if use_graph:
         try:
             warm = torch.cuda.CUDAGraph()
@@ -315,32 +301,22 @@ def run_ours(args, cfg):
                     for _ in range(s0, min(args.steps, s0 + chunk)):
                         step()
                 plain_graphs.append(g)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for s in range(s0, min(args.steps, s0 + chunk)):
-                        step(ev_sets[s])
-                staged_graphs.append(g)
             with torch.cuda.stream(stream):
                 for _ in range(args.warmup):
                     warm.replay()
             stream.synchronize()
         except Exception as e:  # capture unsupported: fall back to eager launches
             print(f"bench: CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
-            use_graph, plain_graphs, staged_graphs = False, [], []
+            use_graph, plain_graphs = False, []
 
-    def run_region(graphs, staged):
+    def timed(fn):
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
             start.record(stream)
-            if use_graph:
-                for g in graphs:
-                    g.replay()
-            else:
-                for s in range(args.steps):
-                    step(ev_sets[s] if staged else None)
+            fn()
             stop.record(stream)
         stream.synchronize()
         torch.cuda.synchronize(dev)
@@ -348,11 +324,17 @@ def run_ours(args, cfg):
             dist.barrier()
         return start.elapsed_time(stop)
 
+    def run_steps():
+        if use_graph:
+            for g in plain_graphs:
+                g.replay()
+        else:
+            for _ in range(args.steps):
+                step()
+
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
     with ClockSampler(gpu_index) as clocks:
-        elapsed_ms = run_region(plain_graphs, False)
-    plan.check()
-    staged_ms = run_region(staged_graphs, True)
+        elapsed_ms = timed(run_steps)
     plan.check()
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
@@ -361,41 +343,58 @@ def run_ours(args, cfg):
     ms_per_step = elapsed_ms / args.steps
     value = cfg.n_ctx * cfg.layers * args.steps * world / (elapsed_ms / 1e3)
 
-    # per-stage kernel times from the events inside the second timed region
-    stage_ms = {s: 0.0 for s in STAGES}
-    attn_ms_by_layer = np.zeros(cfg.layers)
-    for s in range(args.steps):
-        for li in range(cfg.layers):
-            ev = ev_sets[s][li]
-            for i, name in enumerate(STAGES):
-                dt = ev[i].elapsed_time(ev[i + 1])
-                stage_ms[name] += dt
-                if name == "attention":
-                    attn_ms_by_layer[li] += dt
+    # Per-kernel times: one graph per stage holding that stage's kernel for every layer that has
+    # it (cb_blend_stage; each stage rewrites its outputs from its inputs, so replays are idempotent).
+    stage_ms, stage_launches = {}, {}
+    for name in STAGES:
+        layer_ids = [li for li in range(cfg.layers) if stage_applies(name, sizes[li])]
+        if not layer_ids:
+            continue
+
+        def stage_pass(name=name, layer_ids=layer_ids):
+            for li in layer_ids:
+                cb.cb_blend_stage(plan, li + 1, name, cand=None if li == 0 else bufs[li - 1].sel_tok,
+                                  bufs=bufs[li], stream=stream, **d_in[li])
+
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                stage_pass()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            ms = timed(lambda: [g.replay() for _ in range(args.steps)])
+        else:
+            with torch.cuda.stream(stream):
+                stage_pass()
+            ms = timed(lambda: [stage_pass() for _ in range(args.steps)])
+        stage_ms[name] = ms / args.steps
+        stage_launches[name] = len(layer_ids)
+    plan.check()
+
     flops = np.array([attention_flops(cfg, bufs[li].sel_tok[: sizes[li][1]].cpu().numpy())
                       for li in range(cfg.layers)])
     peaks = load_peaks()
     attn_s = stage_ms["attention"] / 1e3
-    achieved_tf = float(flops.sum()) * args.steps / attn_s / 1e12
+    achieved_tf = float(flops.sum()) / attn_s / 1e12
     peak_tf = peaks["bf16_tflops_sustained"]
     traffic = traffic_for("attention.cu")
     roofline = {"kernel": "hkvd_attention", "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                 "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
-                "flops_per_step": float(flops.sum()), "launches_per_step": cfg.layers,
-                "avg_launch_us": 1e3 * stage_ms["attention"] / (args.steps * cfg.layers),
-                "us_by_layer": [round(1e3 * x / args.steps, 2) for x in attn_ms_by_layer]}
+                "flops_per_step": float(flops.sum()), "launches_per_step": stage_launches["attention"],
+                "avg_launch_us": 1e3 * stage_ms["attention"] / stage_launches["attention"]}
     stages = {}
-    for name in STAGES:
-        per_step_ms = stage_ms[name] / args.steps
-        entry = {"ms_per_step": per_step_ms}
-        if name in ("deviation", "fuse", "query_encode"):
+    for name, per_step_ms in stage_ms.items():
+        entry = {"ms_per_step": per_step_ms, "launches_per_step": stage_launches[name],
+                 "us_per_launch": 1e3 * per_step_ms / stage_launches[name]}
+        if name in ("deviation", "fuse"):
             b = sum(stage_bytes(cfg, *sizes[li])[name] for li in range(cfg.layers))
-            if b > 0 and per_step_ms > 0:
-                gbs = b / (per_step_ms / 1e3) / 1e9
-                entry.update({"bytes_per_step": b, "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
+            gbs = b / (per_step_ms / 1e3) / 1e9
+            entry.update({"bytes_per_step": b, "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
         stages[name] = entry
+    launches_per_step = sum(stage_launches.values())
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -404,7 +403,8 @@ def run_ours(args, cfg):
                        "layers": cfg.layers,
                        "l2": f"inputs larger than L2: {sum(sum(t.numel() * 2 for t in d.values()) for d in d_in) / 1e9:.2f} GB per step",
                        "cuda_graph": use_graph, "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": roofline, "stages": stages, "staged_ms_per_step": staged_ms / args.steps,
+            "roofline": roofline, "stages": stages,
+            "stage_sum_ms_per_step": sum(stage_ms.values()),
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary()}
 

@@ -176,16 +176,16 @@ typedef struct cb_layer_io {
  *   selecting layers: deviation over C_l, then top-k -> S_l;
  *   other layers:     S_l = C_l;
  *   then fused K/V for all n_tokens rows in one pass (cached rows re-rotated
- *   by their chunk offset, S_l and suffix rows encoded from k_new / v_new),
- *   the query rows encoded, and the attention. */
+ *   by their chunk offset, S_l and suffix rows encoded from k_new / v_new)
+ *   with the query rows encoded in the same launch, and the attention. */
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream);
 
 /* All layers 1..n_layers of one request (ios[l-1] = buffers of layer l) with
  * the gradual filter wired automatically: layer l reads the candidates
  * ios[l-2].sel_tok (ios[].cand is ignored). Same results as calling
  * cb_blend_layer for each layer in order, but scheduled over streams the plan
- * owns: every layer's deviation, top-k, fused-cache and query-encoding kernels
- * run on one side stream, ahead of the attention, and the attention of
+ * owns: every layer's deviation, top-k and fused-cache (with query encoding)
+ * kernels run on one side stream, ahead of the attention, and the attention of
  * consecutive layers runs on two streams, so that one layer's attention
  * overlaps the next layer's streaming kernels and the tail of the previous
  * attention. All work is ordered after prior work on `stream` and completes
@@ -193,14 +193,22 @@ cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, vo
  * Capturable into a CUDA graph on `stream`. */
 cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios, void* stream);
 
-/* cb_blend_layer with timing marks: events[0..5] are cudaEvent_t handles (any
- * may be NULL) recorded on `stream` before the deviation, before the top-k,
- * before the fused-cache pass, before the query encoding, before the
- * attention and after it (stages a layer skips leave two adjacent marks).
- * Under stream capture they become external event-record nodes. */
-#define CB_N_STAGE_EVENTS 6
-cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                               void* const* events);
+/* The stages of one layer, in the order cb_blend_layer runs them. */
+typedef enum cb_stage {
+  CB_STAGE_DEVIATION = 0, /* V deviation over C_l (selecting layers only) */
+  CB_STAGE_TOPK = 1,      /* top-k of the deviations -> S_l (selecting layers only) */
+  CB_STAGE_FUSE = 2,      /* fused K/V for all n_tokens rows and the encoded query rows, one launch */
+  CB_STAGE_ATTENTION = 3  /* HKVD attention */
+} cb_stage;
+
+/* One stage of cb_blend_layer alone, on `stream`: the kernel cb_blend_layer
+ * launches for that stage, reading what the earlier stages of the same layer
+ * wrote into `io` (run the stages in order, or after a cb_blend_layer of the
+ * layer). A stage the layer does not have (deviation and top-k at layers that
+ * keep their candidates) is a no-op returning CB_OK. Every stage is
+ * idempotent: it rewrites the same outputs from the same inputs. For timing
+ * or profiling one kernel type at a time; capturable into a CUDA graph. */
+cb_status cb_blend_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, int32_t stage, void* stream);
 
 /* HKVD selection that allocates nothing (the pages have no counterpart: this
  * is a deployment aid). For callers that cannot allocate device memory where

@@ -16,7 +16,7 @@ from . import _lib
 from ._lib import CacheBlendError, check
 
 __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_hkvd_topk", "cb_fuse_scatter",
-           "cb_hkvd_attention", "cb_blend_layer", "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check",
+           "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage", "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check",
            "cb_version", "LayerBuffers"]
 
 
@@ -181,17 +181,14 @@ def cb_blend_request(plan, layers, stream=None):
     check(_lib.load().cb_blend_request(plan.handle, n, arr, _stream(stream)))
 
 
-def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None,
-                   events=None):
-    """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer)).
-
-    events: optional sequence of 6 torch.cuda.Event (or None) recorded at the stage
-    boundaries (cb_blend_layer_timed); each event must have been recorded once before
-    so that its CUDA handle exists.
-    """
+def cb_blend_layer(plan, layer, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None):
+    """One layer of the blend; outputs land in `bufs` (sizes from plan.layer_sizes(layer))."""
     io = _layer_io(k_old, v_old, k_new, v_new, q, cand, bufs)
-    if events is None:
-        check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))
-        return
-    arr = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else None) for e in events])
-    check(_lib.load().cb_blend_layer_timed(plan.handle, layer, ctypes.byref(io), _stream(stream), arr))
+    check(_lib.load().cb_blend_layer(plan.handle, layer, ctypes.byref(io), _stream(stream)))
+
+
+def cb_blend_stage(plan, layer, stage, *, k_old, v_old, k_new, v_new, q, cand, bufs: LayerBuffers, stream=None):
+    """One stage ("deviation", "topk", "fuse" or "attention") of cb_blend_layer alone, reading
+    what the layer's earlier stages wrote into `bufs` (cb_blend_stage)."""
+    io = _layer_io(k_old, v_old, k_new, v_new, q, cand, bufs)
+    check(_lib.load().cb_blend_stage(plan.handle, layer, ctypes.byref(io), _lib.STAGES[stage], _stream(stream)))

@@ -18,10 +18,11 @@ CB_OK = 0
 STATUS = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_UNSUPPORTED", 3: "CB_ERR_CUDA",
           4: "CB_ERR_TIMEOUT", 5: "CB_ERR_DEVICE_CHECK"}
 ROPE_STYLES = {"half": 0, "interleaved": 1}
+STAGES = {"deviation": 0, "topk": 1, "fuse": 2, "attention": 3}  # cb_stage
 
 # every symbol include/cacheblend.h declares
 EXPORTS = ("cb_plan_create", "cb_plan_destroy", "cb_layer_sizes", "cb_rope_rerotate", "cb_kv_deviation",
-           "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_blend_layer", "cb_blend_layer_timed",
+           "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage",
            "cb_blend_request",
            "cb_hkvd_select_noalloc", "cb_check", "cb_last_error_string", "cb_version")
 
@@ -68,7 +69,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cb_fuse_scatter": (i32, [vp, vp, vp, vp, vp, vp, i32, vp]),
         "cb_hkvd_attention": (i32, [vp, vp, vp, i32, vp, vp, i32, f32, vp, vp]),
         "cb_blend_layer": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), vp]),
-        "cb_blend_layer_timed": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), vp, ctypes.POINTER(vp)]),
+        "cb_blend_stage": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), i32, vp]),
         "cb_blend_request": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), vp]),
         "cb_hkvd_select_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "cb_check": (i32, [vp]),

@@ -18,7 +18,7 @@ struct cb_plan {
   int32_t n_tokens;
   float2* rope_tab;  // [n_tokens][head_dim / 2]
   int32_t* err;      // [0] flags, [1] first offending index (-1 = none)
-  cudaStream_t aux_stream;  // cb_blend_request: every layer's deviation, top-k, fuse and query encoding
+  cudaStream_t aux_stream;  // cb_blend_request: every layer's deviation, top-k and fuse (with the query encoding)
   cudaStream_t aux_attn;    // cb_blend_request: attention of even layers (odd layers on the caller's stream)
   cudaEvent_t ev_fork, ev_ready, ev_join;
 };
@@ -251,16 +251,6 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                      "cb_hkvd_attention");
 }
 
-static cb_status record_mark(void* const* events, int i, cudaStream_t s) {
-  if (events == nullptr || events[i] == nullptr) return CB_OK;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(s, &cap);
-  if (e == cudaSuccess)
-    e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
-                                 cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
-  return cuda_status(e, "stage event");
-}
-
 struct LayerShape {
   int32_t n_cand, k, mq, selects;
 };
@@ -290,78 +280,65 @@ static cb_status validate_io(cb_plan* plan, int32_t layer, const cb_layer_io* io
   return CB_OK;
 }
 
-// Deviation + top-k (selecting layers), fused cache and query encoding of one layer on `s`.
-// Returns the list S_l the layer's attention reads (`*sel`).
-static cb_status enqueue_streaming(cb_plan* plan, int32_t layer, const cb_layer_io* io, const int32_t* cand,
-                                   const LayerShape& sh, cudaStream_t s, void* const* events, const int32_t** sel_out) {
+// One stage of layer `layer` on `s`; `cand` is the candidate list the layer reads (ignored at
+// layer 1, where the candidates are all context tokens). S_l is sel_tok at selecting layers and
+// the candidates themselves elsewhere; the fuse pass then copies them out to sel_tok / sel_row.
+static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, const int32_t* cand,
+                               const LayerShape& sh, int32_t stage, cudaStream_t s) {
   const auto& c = plan->cfg;
-  const cb::RopeTable t = table(plan);
   if (layer == 1) cand = nullptr;
-  CB_TRY(record_mark(events, 0, s));
-  const int32_t* sel = io->sel_tok;
-  if (sh.selects) {
-    CB_TRY(cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, sh.n_cand, plan->n_ctx, c.hkv,
-                                               c.head_dim, io->dev, plan->err, s),
-                       "deviation"));
-    CB_TRY(record_mark(events, 1, s));
-    CB_TRY(cuda_status(cb::launch_hkvd_topk(io->dev, cand, sh.n_cand, sh.k, io->sel_tok, io->sel_row, plan->err, s),
-                       "top-k"));
-  } else {
-    CB_TRY(record_mark(events, 1, s));
-    sel = cand;  // S_l = C_l: the fuse pass reads the candidates and copies them out
+  const int32_t* sel = sh.selects ? io->sel_tok : cand;
+  switch (stage) {
+    case CB_STAGE_DEVIATION:
+      if (!sh.selects) return CB_OK;
+      return cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, sh.n_cand, plan->n_ctx, c.hkv,
+                                                 c.head_dim, io->dev, plan->err, s),
+                         "deviation");
+    case CB_STAGE_TOPK:
+      if (!sh.selects) return CB_OK;
+      return cuda_status(cb::launch_hkvd_topk(io->dev, cand, sh.n_cand, sh.k, io->sel_tok, io->sel_row, plan->err, s),
+                         "top-k");
+    case CB_STAGE_FUSE: {
+      // One launch: the fused cache and the query encoding (both read the layer's selection list).
+      const bool copy_out = !sh.selects && sh.k > 0;
+      return cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
+                                               sel, sh.k, copy_out ? io->sel_tok : nullptr,
+                                               copy_out ? io->sel_row : nullptr, plan->n_ctx, c.chunk_len,
+                                               plan->n_tokens, c.hkv, c.head_dim, c.rope_style, table(plan),
+                                               sh.mq > 0 ? io->q : nullptr, sh.mq > 0 ? io->q_rot : nullptr, sh.mq,
+                                               c.hq, plan->err, s),
+                         "fuse");
+    }
+    case CB_STAGE_ATTENTION: {
+      if (sh.mq == 0) return CB_OK;
+      // query row t sits at sel[t] (t < k) or n_ctx + t - k
+      const cb::QueryPositions qp{sel, sh.k, plan->n_ctx, true};
+      return cuda_status(cb::launch_hkvd_attention(io->q_rot, qp, sh.mq, io->k_fused, io->v_fused, plan->n_tokens,
+                                                   c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
+                                                   io->out, plan->err, s),
+                         "attention");
+    }
+    default:
+      return fail(CB_ERR_INVALID_ARG, "unknown stage %d", stage);
   }
-  CB_TRY(record_mark(events, 2, s));
-  const bool copy_out = !sh.selects && sh.k > 0;
-  CB_TRY(cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
-                                           sel, sh.k, copy_out ? io->sel_tok : nullptr,
-                                           copy_out ? io->sel_row : nullptr, plan->n_ctx, c.chunk_len,
-                                           plan->n_tokens, c.hkv, c.head_dim, c.rope_style, t, plan->err, s),
-                     "fuse"));
-  CB_TRY(record_mark(events, 3, s));
-  if (sh.mq > 0) {
-    const cb::RowMap im{sel, sh.k, plan->n_ctx, plan->n_tokens};
-    const cb::RowMap om{nullptr, sh.mq, 0, sh.mq};
-    CB_TRY(cuda_status(cb::launch_rope_rows(io->q_rot, io->q, im, om, nullptr, nullptr, nullptr, sh.mq, c.hq,
-                                            c.head_dim, c.rope_style, t, plan->err, s),
-                       "query encode"));
-  }
-  *sel_out = sel;
-  return CB_OK;
 }
 
-// The layer's attention on `s`: query row t sits at sel[t] (t < k) or n_ctx + t - k.
-static cb_status enqueue_attention(cb_plan* plan, const cb_layer_io* io, const int32_t* sel, const LayerShape& sh,
-                                   cudaStream_t s, void* const* events) {
-  const auto& c = plan->cfg;
-  CB_TRY(record_mark(events, 4, s));
-  if (sh.mq > 0) {
-    const cb::QueryPositions qp{sel, sh.k, plan->n_ctx, true};
-    CB_TRY(cuda_status(cb::launch_hkvd_attention(io->q_rot, qp, sh.mq, io->k_fused, io->v_fused, plan->n_tokens,
-                                                 c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
-                                                 io->out, plan->err, s),
-                       "attention"));
-  }
-  return record_mark(events, 5, s);
-}
-
-static cb_status blend_layer_impl(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                                  void* const* events) {
+cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
   CB_TRY(check_plan(plan));
   LayerShape sh;
   CB_TRY(validate_io(plan, layer, io, io ? io->cand : nullptr, &sh));
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t* sel = nullptr;
-  CB_TRY(enqueue_streaming(plan, layer, io, io->cand, sh, s, events, &sel));
-  return enqueue_attention(plan, io, sel, sh, s, events);
+  for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_ATTENTION; ++st)
+    CB_TRY(enqueue_stage(plan, layer, io, io->cand, sh, st, s));
+  return CB_OK;
 }
 
-cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
-  return blend_layer_impl(plan, layer, io, stream, nullptr);
-}
-
-cb_status cb_blend_layer_timed(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream,
-                               void* const* events) {
-  return blend_layer_impl(plan, layer, io, stream, events);
+cb_status cb_blend_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, int32_t stage, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (stage < CB_STAGE_DEVIATION || stage > CB_STAGE_ATTENTION) return fail(CB_ERR_INVALID_ARG, "unknown stage %d", stage);
+  LayerShape sh;
+  CB_TRY(validate_io(plan, layer, io, io ? io->cand : nullptr, &sh));
+  return enqueue_stage(plan, layer, io, io->cand, sh, stage, static_cast<cudaStream_t>(stream));
 }
 
 cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios, void* stream) {
@@ -379,15 +356,15 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
   CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_attn, plan->ev_fork, 0), "fork"));
   for (int32_t l = 1; l <= n_layers; ++l) {
     const cb_layer_io* io = &ios[l - 1];
+    const int32_t* cand = l == 1 ? nullptr : ios[l - 2].sel_tok;
     LayerShape sh;
-    CB_TRY(validate_io(plan, l, io, l == 1 ? nullptr : ios[l - 2].sel_tok, &sh));
-    const int32_t* sel = nullptr;
-    CB_TRY(enqueue_streaming(plan, l, io, l == 1 ? nullptr : ios[l - 2].sel_tok, sh, plan->aux_stream, nullptr,
-                             &sel));
+    CB_TRY(validate_io(plan, l, io, cand, &sh));
+    for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_FUSE; ++st)
+      CB_TRY(enqueue_stage(plan, l, io, cand, sh, st, plan->aux_stream));
     const cudaStream_t a = attn_stream[(l - 1) & 1];
     CB_TRY(cuda_status(cudaEventRecord(plan->ev_ready, plan->aux_stream), "layer inputs ready"));
     CB_TRY(cuda_status(cudaStreamWaitEvent(a, plan->ev_ready, 0), "layer inputs ready"));
-    CB_TRY(enqueue_attention(plan, io, sel, sh, a, nullptr));
+    CB_TRY(enqueue_stage(plan, l, io, cand, sh, CB_STAGE_ATTENTION, a));
   }
   CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, plan->aux_attn), "join"));
   CB_TRY(cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join"));

@@ -428,15 +428,38 @@ __device__ __forceinline__ int warp_lower_bound(const int32_t* sel, int k, int k
   return lo + __popc(__ballot_sync(0xffffffffu, idx < hi && sel[idx] < key));
 }
 
+// Blocks [0, ceil(n_tokens / 8)) build the fused K/V rows; the blocks after them
+// encode the query rows (one warp per row), so the layer's streaming work is
+// one launch.
 template <int STYLE>
 __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
     uint8_t* k_fused, uint8_t* v_fused, const uint8_t* k_old, const uint8_t* v_old, const uint8_t* k_new,
     const uint8_t* v_new, const int32_t* sel, int k, int32_t* out_tok, int32_t* out_row, int n_ctx,
-    int chunk_len, int n_tokens, int hkv, int head_dim, RopeTable t, int32_t* err) {
+    int chunk_len, int n_tokens, int hkv, int head_dim, RopeTable t, const uint8_t* q, uint8_t* q_rot, int mq,
+    int hq, int32_t* err) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ uint8_t is_sel[kFuseRows];
   const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  const int kv_blocks = (n_tokens + kFuseRows - 1) / kFuseRows;
+  if ((int)blockIdx.x >= kv_blocks) {
+    // query row i: token sel[i] (i < k) or n_ctx + i - k, encoded at its own position
+    const int i = ((int)blockIdx.x - kv_blocks) * kFuseRows + warp;
+    if (i >= mq) return;
+    const int tok = i < k ? sel[i] : n_ctx + (i - k);
+    if (tok < 0 || tok >= n_tokens || (i < k && tok >= n_ctx)) {
+      if (lane == 0) record_error(err, kErrIndex, i);
+      return;
+    }
+    if (tok >= t.len) {
+      if (lane == 0) record_error(err, kErrRopeRange, tok);
+      return;
+    }
+    const size_t q_bytes = (size_t)hq * head_dim * 2;
+    rotate_row<STYLE, 2>(q_rot + (size_t)i * q_bytes, q + (size_t)tok * q_bytes, hq, head_dim,
+                         t.tab + (size_t)tok * (head_dim / 2), false, lane);
+    return;
+  }
   const int r0 = blockIdx.x * kFuseRows;
   if (out_tok != nullptr && threadIdx.x < kFuseRows) {
     // a layer that keeps its candidates: S = C is copied out alongside the pass
@@ -582,19 +605,22 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
                               const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
                               int32_t* copy_tok, int32_t* copy_row, int32_t n_ctx, int32_t chunk_len,
                               int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
-                              int32_t* err, cudaStream_t s) {
+                              const void* q, void* q_rot, int32_t mq, int32_t hq, int32_t* err, cudaStream_t s) {
   if (n_tokens <= 0) return cudaSuccess;
-  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows;
+  if (q == nullptr || q_rot == nullptr) mq = 0;
+  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows + (mq + kFuseRows - 1) / kFuseRows;
   auto* kf = (uint8_t*)k_fused;
   auto* vf = (uint8_t*)v_fused;
   if (style == 0)
     return launch_pdl(blend_fuse_kernel<0>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
                       (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
-                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, (const uint8_t*)q, (uint8_t*)q_rot, mq,
+                      hq, err);
   else
     return launch_pdl(blend_fuse_kernel<1>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
                       (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
-                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, err);
+                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, (const uint8_t*)q, (uint8_t*)q_rot, mq,
+                      hq, err);
   return cudaPeekAtLastError();
 }
 

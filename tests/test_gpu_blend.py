@@ -155,3 +155,31 @@ def test_request_scheduling_matches_layer_by_layer(cb, name, layers):
         for f in ("q_rot", "out"):
             assert torch.equal(getattr(a, f)[:mq].view(torch.int16), getattr(b, f)[:mq].view(torch.int16))
     plan.close()
+
+
+def test_stages_one_by_one_match_the_layer_call(cb):
+    # cb_blend_stage runs each stage alone; in order they must give cb_blend_layer's bytes.
+    cfg = get_config("mistral7b")
+    plan = cb.Plan.from_config(cfg)
+    sets = hkvd_noise_sets(cfg)
+    ins = [layer_tensors(generate_layer(cfg, layer, sets)) for layer in (1, 2, 3)]
+    whole = [cb.LayerBuffers(plan) for _ in range(3)]
+    staged = [cb.LayerBuffers(plan) for _ in range(3)]
+    for li in range(3):
+        cb.cb_blend_layer(plan, li + 1, cand=None if li == 0 else whole[li - 1].sel_tok, bufs=whole[li], **ins[li])
+        for stage in ("deviation", "topk", "fuse", "attention"):
+            cb.cb_blend_stage(plan, li + 1, stage, cand=None if li == 0 else staged[li - 1].sel_tok,
+                              bufs=staged[li], **ins[li])
+    torch.cuda.synchronize()
+    plan.check()
+    for li in range(3):
+        _, k, mq, _ = plan.layer_sizes(li + 1)
+        a, b = whole[li], staged[li]
+        assert torch.equal(a.sel_tok[:k], b.sel_tok[:k]) and torch.equal(a.sel_row[:k], b.sel_row[:k])
+        for f in ("k_fused", "v_fused"):
+            assert torch.equal(getattr(a, f).view(torch.int16), getattr(b, f).view(torch.int16))
+        for f in ("q_rot", "out"):
+            assert torch.equal(getattr(a, f)[:mq].view(torch.int16), getattr(b, f)[:mq].view(torch.int16))
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_blend_stage(plan, 1, "fuse", cand=None, bufs=staged[0], **dict(ins[0], q=None))
+    plan.close()
