@@ -21,12 +21,13 @@
 //              is refilled as soon as its S = Q K^T is done);
 //   warp 9     issuer of both products (tcgen05.mma, bf16 in, fp32 accumulate);
 //   warp 10    TMA producer of V tiles (3-stage ring, refilled after P V);
-//   warp 11    the issuer's waiter: it polls the barriers a round of MMAs depends
-//              on and meets the issuer on a named barrier (bar.red.and carries
-//              whether the inputs are ready). A warp that has just
-//              issued MMAs waits 100-200 cycles on its next shared-memory access
-//              (an mbarrier test included) while a named barrier returns at once,
-//              so the issuer itself never touches an mbarrier in the tile loop.
+//   warp 11    the issuer's waiter: it polls the TMA barriers a round of MMAs
+//              depends on; the issuer, the waiter and the softmax warps meet on a
+//              named barrier per tile (the softmax warps once their P is in TMEM).
+//              A warp that has just issued MMAs waits
+//              100-200 cycles on its next shared-memory access (an mbarrier test
+//              included) while a named barrier returns at once, so the issuer
+//              itself never touches an mbarrier in the tile loop.
 // TMEM columns: S in two buffers, tile j in buffer j % 2 at 128 (j % 2) (one
 // N = 128 MMA chain per key tile; WG h reads its 64 columns); each warpgroup
 // writes its P_j (bf16 pairs, 32 columns) over the first half of its own S_j
@@ -68,7 +69,9 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpProducerV = 10;
 constexpr int kWarpWaiter = 11;
-constexpr int kBarIssue = 2;  // named barrier: issuer + waiter (64 threads)
+constexpr int kBarIssue = 2;  // named barrier: issuer + waiter (64 threads), the first round
+constexpr int kBarRound = 3;  // named barrier: the softmax warps + issuer + waiter, once per tile
+constexpr int kRoundThreads = 2 * 128 + 64;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S (fp32) buffer b at 128 b, warpgroup h's half at +64 h (P_j over the first 32
 // columns of that half); O accumulators at 256 + h D.
@@ -85,7 +88,6 @@ struct Bars {
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
   uint64_t s_full[2];   // S_j in TMEM buffer j % 2 (MMA commit); phase j / 2
-  uint64_t p_full[2];   // P_j (both halves) in TMEM buffer j % 2 (eight softmax warps); phase j / 2
   uint64_t pv_done[2];  // P_j V_j accumulated into both O (MMA commit); phase j / 2
   uint64_t drain;
 };
@@ -124,10 +126,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -347,6 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_maxpos;
+  // waiter -> issuer: the TMA inputs of the first round / of round j (slot j % 2) are in shared
+  // memory (0: a wait gave up). Two slots: the waiter's write for round j + 1 cannot overtake the
+  // issuer's read for round j, which precedes its arrival for round j + 1.
+  __shared__ int s_first_ok;
+  __shared__ int s_round_ok[2];
 
   pdl_launch_dependents();
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -373,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bars.s_full[b]), 1);
-      mbar_init(smem_u32(&bars.p_full[b]), 2 * kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(smem_u32(&bars.pv_done[b]), 1);
     }
     mbar_init(smem_u32(&bars.drain), 1);
@@ -458,23 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
     } else if (warp == kWarpMma || warp == kWarpWaiter) {
       // Rounds: round -1 issues S_0 and S_1; round j issues P V_j and then S_{j+2} into the same
-      // buffer. The waiter polls the round's barriers (Q and K_0, K_1; then V_j, K_{j+2} and P_j),
-      // publishes whether they completed, and meets the issuer on named barrier kBarIssue; while
-      // the issuer feeds the tensor core round j, the waiter already polls for round j + 1.
-      // Both warps arrive; every thread gets the AND of the predicates (the waiter's "inputs ready").
-      auto rendezvous = [&](bool ok) -> bool {
-        uint32_t r;
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\t"
-            "setp.ne.u32 p, %1, 0;\n\t"
-            "bar.red.and.pred q, %2, 64, p;\n\t"
-            "selp.u32 %0, 1, 0, q;\n\t}"
-            : "=r"(r)
-            : "r"(ok ? 1u : 0u), "n"(kBarIssue)
-            : "memory");
-        return r != 0;
-      };
-      const int n_rounds = n_kv + 1;
+      // buffer. The waiter polls the TMA barriers a round needs (Q and K_0, K_1; then V_j and
+      // K_{j+2}) and publishes whether they completed; the issuer and the waiter then meet the
+      // softmax warps, whose joining says P_j is in TMEM, on named barrier kBarRound (round -1:
+      // kBarIssue, issuer and waiter only). A named barrier completes within cycles of its last
+      // arrival; an mbarrier polled by a busy warp was noticed hundreds of cycles late.
       if (warp == kWarpWaiter) {
         auto spin_all = [&](uint32_t bar, uint32_t parity, int site) -> bool {
           return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site));
@@ -482,16 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto k_ready = [&](int j) {
           return spin_all(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, 11);
         };
-        for (int rd = -1; rd + 1 < n_rounds; ++rd) {
-          bool ok;
-          if (rd < 0) {
-            ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0) && (n_kv < 2 || k_ready(1));
-          } else {
-            const int j = rd;
-            ok = spin_all(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, 13) &&
-                 (j + 2 >= n_kv || k_ready(j + 2)) && spin_all(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, 12);
-          }
-          if (!rendezvous(ok)) break;
+        bool ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0) && (n_kv < 2 || k_ready(1));
+        if (lane == 0) s_first_ok = ok ? 1 : 0;
+        asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
+        for (int j = 0; j < n_kv; ++j) {
+          // every round is joined, also after a failure (the issuer then skips its MMAs)
+          ok = ok && spin_all(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, 13) &&
+               (j + 2 >= n_kv || k_ready(j + 2));
+          if (lane == 0) s_round_ok[j & 1] = ok ? 1 : 0;
+          asm volatile("bar.sync %0, %1;" ::"n"(kBarRound), "n"(kRoundThreads) : "memory");
         }
       } else {
         constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false);
@@ -512,32 +501,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(smem_u32(&bars.k_empty[st]));
           tc_commit(smem_u32(&bars.s_full[b]));
         };
-        for (int rd = -1; rd + 1 < n_rounds; ++rd) {
-          if (!rendezvous(true)) break;
+        asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
+        bool ok = s_first_ok != 0;
+        if (ok) {
           tc_fence_after();
-          if (rd < 0) {
-            if (elect_one()) {
-              issue_s(0);
-              if (n_kv > 1) issue_s(1);
-            }
-          } else {
-            // O_h += P_{j,h} V_{j,h} for both halves h, then S_{j+2} into the same buffer
-            // (executed after this P V, which reads P_j from it).
-            const int j = rd, b = j & 1, st = j % kVStages;
-            const uint64_t dv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
-            const uint32_t acc0 = j > 0 ? 1u : 0u;
-            if (elect_one()) {
+          if (elect_one()) {
+            issue_s(0);
+            if (n_kv > 1) issue_s(1);
+          }
+          __syncwarp();
+        }
+        for (int j = 0; j < n_kv; ++j) {
+          asm volatile("bar.sync %0, %1;" ::"n"(kBarRound), "n"(kRoundThreads) : "memory");
+          ok = ok && s_round_ok[j & 1] != 0 && !*abort_flag;
+          if (!ok) continue;
+          tc_fence_after();
+          // O_h += P_{j,h} V_{j,h} for both halves h, then S_{j+2} into the same buffer
+          // (executed after this P V, which reads P_j from it).
+          const int b = j & 1, st = j % kVStages;
+          const uint64_t dv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int ks = 0; ks < kHalf / 16; ++ks)
-                  mma_ts(tmem + col_o(h, D), tmem + col_s(b, h) + ks * 8,
-                         dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
-              }
-              tc_commit(smem_u32(&bars.v_empty[st]));
-              tc_commit(smem_u32(&bars.pv_done[b]));
-              if (j + 2 < n_kv) issue_s(j + 2);
+              for (int ks = 0; ks < kHalf / 16; ++ks)
+                mma_ts(tmem + col_o(h, D), tmem + col_s(b, h) + ks * 8,
+                       dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
             }
+            tc_commit(smem_u32(&bars.v_empty[st]));
+            tc_commit(smem_u32(&bars.pv_done[b]));
+            if (j + 2 < n_kv) issue_s(j + 2);
           }
           __syncwarp();
         }
@@ -561,13 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w = mbar_spin(smem_u32(&bars.pv_done[j & 1]), (j >> 1) & 1, abort_flag, p.err, site);
       return __all_sync(0xffffffffu, w);
     };
-    for (int j = 0; j < n_kv; ++j) {
+    // One tile; false if a wait gave up (the abort flag is raised then).
+    auto tile = [&](int j) -> bool {
       const int b = j & 1;
-      const bool w = mbar_spin(smem_u32(&bars.s_full[b]), (j >> 1) & 1, abort_flag, p.err, 20 + wg);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.s_full[b]), (j >> 1) & 1, abort_flag, p.err, 20 + wg)))
+        return false;
       tc_fence_after();
       // Copy this half's 64 scores to registers; P_j is later written over their first 32 columns.
       uint32_t sv[kHalf];
@@ -610,10 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // O holds this warpgroup's sum through tile j - 1: wait for that P V, then scale it.
         if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
-          if (!wait_pv(j - 1, 22 + wg)) {
-            ok = false;
-            break;
-          }
+          if (!wait_pv(j - 1, 22 + wg)) return false;
           tc_fence_after();
           const float a = scale_o ? alpha : 1.0f;
 #pragma unroll 1
@@ -650,9 +639,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_x32(lane_base + col_s(b, wg), pk);
       tmem_st_wait();
+      return true;
+    };
+    // Every softmax warp syncs on kBarRound once per key tile, also after a failed wait (then
+    // without work), so every round of the issuer and its waiter completes. A blocking sync, not
+    // an arrival: a warp cannot reach the next round's barrier before this round's has completed,
+    // so no arrival is ever counted in the wrong round. It costs little: the next tile needs
+    // S_{j+1}, which the issuer finishes issuing just before it joins this barrier.
+    for (int j = 0; j < n_kv; ++j) {
+      if (ok) ok = tile(j);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.p_full[b]));
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarRound), "n"(kRoundThreads) : "memory");
     }
     if (ok) ok = wait_pv(n_kv - 1, 26 + wg);
     // Merge the two warpgroups' partial results; each writes half of the columns.
