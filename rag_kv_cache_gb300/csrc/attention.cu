@@ -394,6 +394,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The query rows, positions and fused K/V come from the kernels before this one on the stream.
   if (p.wait_prior) pdl_wait();
 
+  // Q and the first K and V tiles do not depend on the query positions (every query tile sees
+  // key tile 0): their loads start before the positions are read.
+  if (warp == kWarpProducer && lane == 0) {
+    const uint32_t qb = smem_u32(&bars.q_full);
+    mbar_expect_tx(qb, kQBytes);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b) tma_load_4d(sQ + b * kQBox, &tm_q, qb, b * 64, 0, g, t0);
+    const uint32_t kb = smem_u32(&bars.k_full[0]);
+    mbar_expect_tx(kb, kKVBytes);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b) tma_load_3d(sK0 + b * kKVBox, &tm_k, kb, b * 64, g, 0);
+  } else if (warp == kWarpProducerV && lane == 0) {
+    const uint32_t vb = smem_u32(&bars.v_full[0]);
+    mbar_expect_tx(vb, kKVBytes);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b) tma_load_3d(sV0 + b * kKVBox, &tm_v, vb, b * 64, g, 0);
+  }
+
   // Query position of each softmax thread's row; padded rows repeat the tile's last token.
   int my_pos = 0;
   if (threadIdx.x < 2 * kSoftmaxThreads) {
@@ -422,11 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2 * (kSoftmaxThreads / 32)) {
     if (warp == kWarpProducer && lane == 0) {
       const uint32_t qb = smem_u32(&bars.q_full);
-      mbar_expect_tx(qb, kQBytes);
-#pragma unroll
-      for (int b = 0; b < kBoxes; ++b) tma_load_4d(sQ + b * kQBox, &tm_q, qb, b * 64, 0, g, t0);
-      int nk = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      int nk = 1;  // Q and K tile 0 are in flight already
+      for (int j = 1; j < n_kv; ++j) {
         const int sk = j % kKStages;
         if (j >= kKStages &&
             !mbar_wait(smem_u32(&bars.k_empty[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1))
@@ -443,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = nk - kKStages < 0 ? 0 : nk - kKStages; j < nk; ++j)
         mbar_wait(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 4, false);
     } else if (warp == kWarpProducerV && lane == 0) {
-      int nv = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      int nv = 1;  // V tile 0 is in flight already
+      for (int j = 1; j < n_kv; ++j) {
         const int sv = j % kVStages;
         if (j >= kVStages &&
             !mbar_wait(smem_u32(&bars.v_empty[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2))
@@ -474,12 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0) && (n_kv < 2 || k_ready(1));
         if (lane == 0) s_first_ok = ok ? 1 : 0;
+        // bar.sync is warp-aligned: the warp must reach it converged, not split by the lane-0
+        // store above (a split warp's arrivals can be counted in the wrong phase).
+        __syncwarp();
         asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
         for (int j = 0; j < n_kv; ++j) {
           // every round is joined, also after a failure (the issuer then skips its MMAs)
           ok = ok && spin_all(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, 13) &&
                (j + 2 >= n_kv || k_ready(j + 2));
           if (lane == 0) s_round_ok[j & 1] = ok ? 1 : 0;
+          __syncwarp();
           asm volatile("bar.sync %0, %1;" ::"n"(kBarRound), "n"(kRoundThreads) : "memory");
         }
       } else {
@@ -501,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(smem_u32(&bars.k_empty[st]));
           tc_commit(smem_u32(&bars.s_full[b]));
         };
+        __syncwarp();
         asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
         bool ok = s_first_ok != 0;
         if (ok) {
@@ -512,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         for (int j = 0; j < n_kv; ++j) {
+          __syncwarp();
           asm volatile("bar.sync %0, %1;" ::"n"(kBarRound), "n"(kRoundThreads) : "memory");
           ok = ok && s_round_ok[j & 1] != 0 && !*abort_flag;
           if (!ok) continue;
@@ -660,6 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_ml[wg][0][r] = m_ref;
     s_ml[wg][1][r] = l;
     tc_fence_before();
+    __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
     ok = ok && !*abort_flag;
     if (__all_sync(0xffffffffu, ok)) {
