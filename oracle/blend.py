@@ -14,7 +14,14 @@ Gradual filter ("rag的kvcache问题" §渐进式过滤机制), as read here:
   layer 2: candidates = the layer-1 selection, keep k_2 = floor(r2 * n_ctx / 100);
   layer >= 3: candidates = the previous selection, which is kept whole
               (no deviation, no top-k).
+A second reading (filter="reselect"), which the page leaves open: the
+layer-2 step repeats at every layer >= 2, i.e. candidates = the layer-1
+selection and k_2 kept by that layer's own deviation; the page's "stable from
+layer 3" is then an observation about the selections, not a rule.
 A single-layer workload runs layer 1 with r1 as its ratio.
+
+Deviation ("deviation" argument): "v" ranks by the V distance of
+"数学推导" §近似解, "kv" by the K+V distance (see oracle.deviation).
 """
 
 from __future__ import annotations
@@ -24,15 +31,21 @@ from dataclasses import dataclass
 import numpy as np
 
 from .attention import causal_gqa_attention
-from .deviation import bf16_bits_to_f64, deviation_canonical_f32
+from .deviation import bf16_bits_to_f64, deviation_canonical_f32, kv_deviation_canonical_f32
 from .fuse import fused_kv
 from .positions import chunk_local_positions, global_positions
 from .rope import rerotate, rope_rotate, round_bf16
 from .topk import hkvd_topk, k_for_ratio
 
 
-def gradual_filter_schedule(n_ctx: int, layers: int, r1_pct: int, r2_pct: int):
+FILTERS = ("keep", "reselect")
+DEVIATIONS = ("v", "kv")
+
+
+def gradual_filter_schedule(n_ctx: int, layers: int, r1_pct: int, r2_pct: int, filter: str = "keep"):
     """[(layer, k_l, selects)] for layers 1..layers."""
+    if filter not in FILTERS:
+        raise ValueError(f"unknown filter {filter!r}")
     if not 0 <= r2_pct <= r1_pct <= 100:
         raise ValueError("need 0 <= r2 <= r1 <= 100")
     k1, k2 = k_for_ratio(r1_pct, n_ctx), k_for_ratio(r2_pct, n_ctx)
@@ -43,8 +56,15 @@ def gradual_filter_schedule(n_ctx: int, layers: int, r1_pct: int, r2_pct: int):
         elif layer == 2:
             out.append((2, k2, True))
         else:
-            out.append((layer, k2, False))
+            out.append((layer, k2, filter == "reselect"))
     return out
+
+
+def candidate_layer(layer: int, filter: str = "keep") -> int:
+    """The layer whose selection is C_l (0: all context tokens)."""
+    if layer <= 1:
+        return 0
+    return 1 if filter == "reselect" else layer - 1
 
 
 @dataclass
@@ -65,7 +85,7 @@ class LayerResult:
 
 
 def blend_layer(cfg, inp, layer: int, cand, k: int, selects: bool, style: str = "half",
-                attention_rows=None) -> LayerResult:
+                attention_rows=None, deviation: str = "v") -> LayerResult:
     """One layer. `inp` is a workloads.LayerInputs; attention_rows=None computes all
     query rows, an index array computes only those rows, and False skips attention."""
     n_ctx, n = cfg.n_ctx, cfg.n_tokens
@@ -74,7 +94,13 @@ def blend_layer(cfg, inp, layer: int, cand, k: int, selects: bool, style: str = 
     p_old = chunk_local_positions(cfg.n_chunks, cfg.chunk_len)
 
     if selects:
-        dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
+        if deviation == "v":
+            dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
+        elif deviation == "kv":
+            dev = kv_deviation_canonical_f32(inp.k_new[cand], inp.k_old[cand], inp.v_new[cand], inp.v_old[cand],
+                                             p_old[cand], cfg.rope_theta, style)
+        else:
+            raise ValueError(f"unknown deviation {deviation!r}")
         sel_tok, sel_row = hkvd_topk(dev, cand, k)
     else:
         if k != cand.size:
@@ -103,17 +129,19 @@ def blend_layer(cfg, inp, layer: int, cand, k: int, selects: bool, style: str = 
     return LayerResult(layer, cand, k, dev, sel_tok, sel_row, k_f, v_f, is_new, q_tok, q_rot, out, vs)
 
 
-def blend_request(cfg, layer_inputs, style: str = "half", attention_rows=None):
+def blend_request(cfg, layer_inputs, style: str = "half", attention_rows=None, deviation: str = "v",
+                  filter: str = "keep"):
     """Run the gradual filter over the layers whose inputs are given (in order from layer 1).
 
     layer_inputs: iterable of workloads.LayerInputs for layers 1, 2, ...
     Yields one LayerResult per layer.
     """
-    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
-    cand = np.arange(cfg.n_ctx, dtype=np.int64)
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct, filter)
+    sel = {0: np.arange(cfg.n_ctx, dtype=np.int64)}
     for (layer, k, selects), inp in zip(sched, layer_inputs):
         if inp.layer != layer:
             raise ValueError("layer inputs must start at layer 1 and be consecutive")
-        res = blend_layer(cfg, inp, layer, cand, k, selects, style, attention_rows)
-        cand = res.sel_tok
+        cand = sel[candidate_layer(layer, filter)]
+        res = blend_layer(cfg, inp, layer, cand, k, selects, style, attention_rows, deviation)
+        sel[layer] = res.sel_tok
         yield res

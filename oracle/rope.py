@@ -15,6 +15,8 @@ Which two of the D coordinates form pair j is not fixed by the pages:
 
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 STYLES = ("half", "interleaved")
@@ -57,6 +59,32 @@ def rerotate(k_old: np.ndarray, p_old, p_new, theta: float, style: str = "half")
     """Move keys encoded at p_old to p_new: R_{p_new - p_old} k_old."""
     delta = np.asarray(p_new, dtype=np.int64) - np.asarray(p_old, dtype=np.int64)
     return rope_rotate(k_old, delta, theta, style)
+
+
+def rope_table_f32(positions, head_dim: int, theta: float):
+    """fl32(cos a), fl32(sin a) of every pair j at every given position, [n, D/2] each.
+
+    a = fl64(p * fl64(theta^(-2j/D))) with the exponent formed as (-2 j) / D
+    in fp64, and theta^x, cos and sin from the C library's fp64 routines
+    (Python's math module calls them one value at a time). The result is the
+    per-pair rotation that fp32 RoPE arithmetic starts from; where a
+    computation must be reproduced bit for bit in fp32, it starts here.
+    """
+    pos = [int(p) for p in np.asarray(positions).reshape(-1)]
+    half = head_dim // 2
+    inv = [math.pow(float(theta), (-2.0 * j) / head_dim) for j in range(half)]
+    cos_t = np.empty((len(pos), half), np.float32)
+    sin_t = np.empty((len(pos), half), np.float32)
+    cache = {}
+    for r, p in enumerate(pos):
+        row = cache.get(p)
+        if row is None:
+            ang = [float(p) * f for f in inv]
+            row = (np.array([math.cos(a) for a in ang], np.float64).astype(np.float32),
+                   np.array([math.sin(a) for a in ang], np.float64).astype(np.float32))
+            cache[p] = row
+        cos_t[r], sin_t[r] = row
+    return cos_t, sin_t
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

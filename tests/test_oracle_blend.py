@@ -6,7 +6,7 @@ import dataclasses
 import numpy as np
 import torch
 
-from oracle.blend import blend_layer, blend_request, gradual_filter_schedule
+from oracle.blend import blend_layer, blend_request, candidate_layer, gradual_filter_schedule
 from oracle.deviation import bf16_bits_to_f64
 from oracle.rope import rerotate, rope_rotate, round_bf16
 from oracle.topk import k_for_ratio
@@ -103,3 +103,46 @@ def test_workload_generator_is_deterministic_and_shaped():
         assert np.array_equal(getattr(a, f), getattr(b, f))
     assert a.k_old.shape == (512, 2, 64) and a.k_new.shape == (544, 2, 64) and a.q.shape == (544, 4, 64)
     assert a.hkvd_set.size == 76
+
+
+def test_reselect_schedule_and_candidate_layers():
+    s = gradual_filter_schedule(3072, 32, 30, 15, filter="reselect")
+    assert s[0] == (1, 921, True) and all(x == (i + 2, 460, True) for i, x in enumerate(s[1:]))
+    assert [candidate_layer(l, "reselect") for l in (1, 2, 3, 9)] == [0, 1, 1, 1]
+    assert [candidate_layer(l, "keep") for l in (1, 2, 3, 9)] == [0, 1, 2, 8]
+
+
+def test_reselect_follows_each_layers_high_deviation_set():
+    # With filter="reselect" every layer >= 2 re-ranks the layer-1 pool by its own deviation,
+    # so it keeps the tokens of that layer's high-noise set that lie in the pool (the noise
+    # model: sigma 1.0 on the set, 0.01 elsewhere, 10% of the set swapped per layer).
+    cfg = dataclasses.replace(_small_multilayer(), name="small4r", config_id=92, layers=5)
+    from workloads.generator import hkvd_noise_sets
+    sets = hkvd_noise_sets(cfg)
+    inputs = [generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1)]
+    res = list(blend_request(cfg, iter(inputs), attention_rows=False, filter="reselect"))
+    pool = set(res[0].sel_tok.tolist())
+    k2 = k_for_ratio(cfg.r2_pct, cfg.n_ctx)
+    moved = False
+    for layer in range(2, cfg.layers + 1):
+        r = res[layer - 1]
+        assert np.array_equal(r.cand, res[0].sel_tok) and r.dev is not None and r.sel_tok.size == k2
+        want = pool & set(sets[layer - 1].tolist())
+        assert len(want) <= k2 and want <= set(r.sel_tok.tolist())
+        moved |= not np.array_equal(r.sel_tok, res[1].sel_tok)
+    assert moved  # the keep reading would have frozen S_2
+
+
+def test_kv_deviation_mode_ranks_by_the_kv_number():
+    cfg = _small_multilayer()
+    inp = generate_layer(cfg, 1)
+    from oracle.deviation import kv_deviation_canonical_f32
+    from oracle.positions import chunk_local_positions
+    cand = np.arange(cfg.n_ctx)
+    k = k_for_ratio(cfg.r1_pct, cfg.n_ctx)
+    res = blend_layer(cfg, inp, 1, cand, k, True, attention_rows=False, deviation="kv")
+    dev = kv_deviation_canonical_f32(inp.k_new[:cfg.n_ctx], inp.k_old, inp.v_new[:cfg.n_ctx], inp.v_old,
+                                     chunk_local_positions(cfg.n_chunks, cfg.chunk_len), cfg.rope_theta)
+    np.testing.assert_array_equal(res.dev.view(np.uint32), dev.view(np.uint32))
+    kth = np.sort(dev)[::-1][k - 1]
+    assert np.all(dev[res.sel_tok] >= kth) and np.sum(dev > kth) <= k
