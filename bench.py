@@ -59,6 +59,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--deviation", choices=["v", "kv"], default="v",
+                    help="rank by the V deviation (default) or by the K+V deviation")
+    ap.add_argument("--filter", choices=["keep", "reselect"], default="keep",
+                    help="layers >= 3 keep S_{l-1} (default) or re-select from the layer-1 pool")
     return ap.parse_args()
 
 
@@ -147,34 +151,42 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- oracle (CPU)
-def oracle_chain(cfg, inputs):
+def oracle_chain(cfg, inputs, deviation="v", filter="keep"):
     """Candidate lists of every layer (the oracle's own selection chain)."""
-    from oracle.blend import gradual_filter_schedule
-    from oracle.deviation import deviation_canonical_f32
+    from oracle.blend import candidate_layer, gradual_filter_schedule
+    from oracle.deviation import deviation_canonical_f32, kv_deviation_canonical_f32
+    from oracle.positions import chunk_local_positions
     from oracle.topk import hkvd_topk
 
-    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
-    cand = np.arange(cfg.n_ctx)
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct, filter)
+    p_old = chunk_local_positions(cfg.n_chunks, cfg.chunk_len)
+    sels = {0: np.arange(cfg.n_ctx)}
     chain = []
     for (layer, k, selects), inp in zip(sched, inputs):
+        cand = sels[candidate_layer(layer, filter)]
         chain.append((layer, cand, k, selects))
+        sels[layer] = cand
         if selects:
-            dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
-            cand, _ = hkvd_topk(dev, cand, k)
+            if deviation == "kv":
+                dev = kv_deviation_canonical_f32(inp.k_new[cand], inp.k_old[cand], inp.v_new[cand], inp.v_old[cand],
+                                                 p_old[cand], cfg.rope_theta)
+            else:
+                dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
+            sels[layer], _ = hkvd_topk(dev, cand, k)
     return chain
 
 
-def time_oracle_layer(cfg, inp, layer, cand, k, selects):
+def time_oracle_layer(cfg, inp, layer, cand, k, selects, deviation="v"):
     from oracle.blend import blend_layer
 
     t0 = time.perf_counter()
-    blend_layer(cfg, inp, layer, cand, k, selects)
+    blend_layer(cfg, inp, layer, cand, k, selects, deviation=deviation)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, inputs):
-    chain = oracle_chain(cfg, inputs[:3])
-    times = [time_oracle_layer(cfg, inputs[i], *chain[i]) for i in range(min(3, cfg.layers))]
+def cpu_baseline(cfg, inputs, deviation="v", filter="keep"):
+    chain = oracle_chain(cfg, inputs[:3], deviation, filter)
+    times = [time_oracle_layer(cfg, inputs[i], *chain[i], deviation) for i in range(min(3, cfg.layers))]
     if cfg.layers >= 3:
         t_step = times[0] + times[1] + (cfg.layers - 2) * times[2]
         sample = (f"oracle on layers 1, 2, 3 of {cfg.name} (all query rows); per-step time extrapolated as "
@@ -194,19 +206,20 @@ def run_reference(args, cfg):
         return 0
     sets = hkvd_noise_sets(cfg)
     inputs = [generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1)]
-    chain = oracle_chain(cfg, inputs)
+    chain = oracle_chain(cfg, inputs, args.deviation, args.filter)
     for i in range(args.warmup):
-        time_oracle_layer(cfg, inputs[i % cfg.layers], *chain[i % cfg.layers])
+        time_oracle_layer(cfg, inputs[i % cfg.layers], *chain[i % cfg.layers], args.deviation)
     total = 0.0
     for i in range(args.steps):
         j = (args.warmup + i) % cfg.layers
-        total += time_oracle_layer(cfg, inputs[j], *chain[j])
+        total += time_oracle_layer(cfg, inputs[j], *chain[j], args.deviation)
     value = cfg.n_ctx * args.steps / total
     sample = f"each step one whole layer of {cfg.name} by the CPU oracle, cycling through its {cfg.layers} layers"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": data_desc(cfg), "config": {"workload": workload_desc(cfg), "n_ctx": cfg.n_ctx},
+            "data": data_desc(cfg), "config": {"workload": workload_desc(cfg), "n_ctx": cfg.n_ctx,
+                                               "deviation": args.deviation, "filter": args.filter},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -220,13 +233,14 @@ def attention_flops(cfg, sel_tok):
     return 4.0 * cfg.hq * cfg.head_dim * float(np.sum(q_pos + 1))
 
 
-def stage_bytes(cfg, n_cand, k, mq, selects):
+def stage_bytes(cfg, n_cand, k, mq, selects, deviation="v"):
     """Algorithmic HBM bytes of one layer's streaming kernels: deviation reads V_new and V_old of
-    the candidates; the fuse pass reads and writes K and V of every row and reads and writes the
-    query rows it encodes."""
+    the candidates (and K_new, K_old for the K+V deviation); the fuse pass reads and writes K and
+    V of every row and reads and writes the query rows it encodes."""
     row_kv = cfg.hkv * cfg.head_dim * 2
     row_q = cfg.hq * cfg.head_dim * 2
-    return {"deviation": 2.0 * n_cand * row_kv if selects else 0.0,
+    reads = 4.0 if deviation == "kv" else 2.0
+    return {"deviation": reads * n_cand * row_kv if selects else 0.0,
             "fuse": 4.0 * cfg.n_tokens * row_kv + 2.0 * mq * row_q}
 
 
@@ -269,8 +283,12 @@ def run_ours(args, cfg):
     sets = hkvd_noise_sets(cfg)
     host_inputs = [generate_layer(cfg, layer, sets) for layer in range(1, cfg.layers + 1)]
     d_in = [layer_tensors(inp, dev) for inp in host_inputs]
-    plan = cb.Plan.from_config(cfg)
+    plan = cb.Plan.from_config(cfg, deviation=args.deviation, filter=args.filter)
     bufs = [cb.LayerBuffers(plan, dev) for _ in range(cfg.layers)]
+
+    def cand_of(li):  # C of layer li + 1: the selection of the layer the plan's filter names
+        c = plan.candidate_layer(li + 1)
+        return None if c == 0 else bufs[c - 1].sel_tok
     sizes = [plan.layer_sizes(layer) for layer in range(1, cfg.layers + 1)]
     stream = torch.cuda.Stream(dev)
 
@@ -353,8 +371,7 @@ def run_ours(args, cfg):
 
         def stage_pass(name=name, layer_ids=layer_ids):
             for li in layer_ids:
-                cb.cb_blend_stage(plan, li + 1, name, cand=None if li == 0 else bufs[li - 1].sel_tok,
-                                  bufs=bufs[li], stream=stream, **d_in[li])
+                cb.cb_blend_stage(plan, li + 1, name, cand=cand_of(li), bufs=bufs[li], stream=stream, **d_in[li])
 
         if use_graph:
             g = torch.cuda.CUDAGraph()
@@ -390,7 +407,7 @@ def run_ours(args, cfg):
         entry = {"ms_per_step": per_step_ms, "launches_per_step": stage_launches[name],
                  "us_per_launch": 1e3 * per_step_ms / stage_launches[name]}
         if name in ("deviation", "fuse"):
-            b = sum(stage_bytes(cfg, *sizes[li])[name] for li in range(cfg.layers))
+            b = sum(stage_bytes(cfg, *sizes[li], args.deviation)[name] for li in range(cfg.layers))
             gbs = b / (per_step_ms / 1e3) / 1e9
             entry.update({"bytes_per_step": b, "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
         stages[name] = entry
@@ -400,7 +417,7 @@ def run_ours(args, cfg):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": data_desc(cfg),
             "config": {"workload": workload_desc(cfg), "n_ctx": cfg.n_ctx, "n_tokens": cfg.n_tokens,
-                       "layers": cfg.layers,
+                       "layers": cfg.layers, "deviation": args.deviation, "filter": args.filter,
                        "l2": f"inputs larger than L2: {sum(sum(t.numel() * 2 for t in d.values()) for d in d_in) / 1e9:.2f} GB per step",
                        "cuda_graph": use_graph, "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "stages": stages,
@@ -411,7 +428,7 @@ def run_ours(args, cfg):
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, host_inputs[:3])
+        line["cpu_baseline"] = cpu_baseline(cfg, host_inputs[:3], args.deviation, args.filter)
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
@@ -449,13 +466,13 @@ def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
                 for k, t in h_in[li].items():
                     d_in[li][k].copy_(t, non_blocking=True)
                 copied[li].record(h2d)
-        cand = None
         for li in range(cfg.layers):
             comp.wait_event(copied[li])
             comp.wait_event(drained[li])
-            cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=bufs[li], stream=comp, **d_in[li])
+            c = plan.candidate_layer(li + 1)
+            cb.cb_blend_layer(plan, li + 1, cand=None if c == 0 else bufs[c - 1].sel_tok, bufs=bufs[li],
+                              stream=comp, **d_in[li])
             layer_done[li].record(comp)
-            cand = bufs[li].sel_tok
             with torch.cuda.stream(d2h):
                 d2h.wait_event(layer_done[li])
                 h_out[li].copy_(bufs[li].out[: sizes[li][2]], non_blocking=True)

@@ -65,6 +65,20 @@ typedef enum cb_rope_style {
   CB_ROPE_INTERLEAVED = 1  /* (2j, 2j + 1) */
 } cb_rope_style;
 
+/* What the HKVD selection ranks. */
+typedef enum cb_deviation {
+  CB_DEV_V = 0,  /* ||V_new - V_old||^2 ("数学推导" §近似解) */
+  CB_DEV_KV = 1  /* ||K~_new - K~_old||^2 + ||V_new - V_old||^2: the deviation on the whole KV of
+                    "rag的kvcache问题" §核心发现, keys compared at the same position (below) */
+} cb_deviation;
+
+/* Which tokens a layer after layer 2 chooses from ("rag的kvcache问题" §渐进式过滤机制
+ * fixes layers 1 and 2; later layers are read two ways). */
+typedef enum cb_filter {
+  CB_FILTER_KEEP = 0,     /* layer >= 3 keeps S_{l-1} whole: no deviation, no top-k */
+  CB_FILTER_RESELECT = 1  /* every layer >= 2 ranks the layer-1 pool S_1 by its own deviation, keeps k_2 */
+} cb_filter;
+
 /* One blend request: n_chunks cached chunks of chunk_len tokens (chunk-local
  * positions 0 .. chunk_len-1), then n_suffix uncached query tokens. Token i of
  * the request sits at global position i. r1_pct / r2_pct: gradual-filter
@@ -80,13 +94,17 @@ typedef struct cb_config {
   int32_t rope_style;  /* cb_rope_style */
   int32_t r1_pct;      /* layer-1 keep ratio, 0..100 */
   int32_t r2_pct;      /* keep ratio from layer 2 on, 0..r1_pct */
+  int32_t deviation;   /* cb_deviation */
+  int32_t filter;      /* cb_filter */
 } cb_config;
 
 typedef struct cb_plan cb_plan;
 
 /* Create a plan on the current device: copies *cfg, builds the RoPE cos/sin
- * table for positions 0 .. n_tokens-1 (fp64 angles rounded to fp32), the
- * device error word and the side streams of cb_blend_request. Synchronous. */
+ * table for positions 0 .. n_tokens-1 on the host (angle p * theta^(-2j/D) in
+ * fp64 with the C library's pow, cos and sin, rounded to fp32) and copies it
+ * to the device, and creates the device error word and the side streams of
+ * cb_blend_request. Synchronous. */
 cb_status cb_plan_create(const cb_config* cfg, cb_plan** out);
 
 /* Free everything the plan owns. Waits for the device first. NULL is a no-op. */
@@ -96,7 +114,9 @@ cb_status cb_plan_destroy(cb_plan* plan);
  * n_cand = |C_l| (candidates read), k = |S_l| (kept), mq = k + n_suffix
  * (attention query rows), selects = 1 if the layer runs deviation + top-k.
  * Layer 1: C = all n_ctx tokens, k = floor(r1 * n_ctx / 100). Layer 2: C = S_1,
- * k = floor(r2 * n_ctx / 100). Layer >= 3: C = S_{l-1}, kept whole. */
+ * k = floor(r2 * n_ctx / 100). Layer >= 3: C = S_{l-1}, kept whole
+ * (CB_FILTER_KEEP), or C = S_1 and k = floor(r2 * n_ctx / 100) selected again
+ * (CB_FILTER_RESELECT). */
 cb_status cb_layer_sizes(const cb_plan* plan, int32_t layer, int32_t* n_cand, int32_t* k,
                          int32_t* mq, int32_t* selects);
 
@@ -125,6 +145,21 @@ cb_status cb_rope_rerotate(cb_plan* plan, void* out, const void* x, const int32_
  * Candidates outside [0, n_ctx) are skipped (dev = NaN, CB_ERR_DEVICE_CHECK). */
 cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, const int32_t* cand,
                           int32_t m, float* dev, void* stream);
+
+/* K+V deviation (CB_DEV_KV): for i in [0, m), t = cand ? cand[i] : i,
+ *   dev[i] = sum_{h,j} (R_{p_new} k_new[t] - R_{p_new - p_old} k_old[t])[h,j]^2
+ *          + sum_{h,j} (v_new[t, h, j] - v_old[t, h, j])^2,
+ * with p_old = t mod chunk_len (the cached key's chunk-local position) and
+ * k_new the recomputed key before RoPE. Rotations keep lengths, so the key
+ * term is computed as ||R_{p_old} k_new[t] - k_old[t]||^2 (one turn): each
+ * element of R_{p_old} k_new in fp32 from the plan's table row p_old, first
+ * pair member fl(fl(x c) - fl(y s)), second fl(fl(x s) + fl(y c)), then the
+ * canonical order of cb_kv_deviation over the sequence [key part padded to a
+ * multiple of 256 elements, V part padded the same way]: every lane adds its
+ * key chunks, then its V chunks. Same layouts and error behaviour as
+ * cb_kv_deviation; k_new / k_old [>= t+1, hkv, D] by token. */
+cb_status cb_kv_deviation_kv(cb_plan* plan, const void* k_new, const void* k_old, const void* v_new,
+                             const void* v_old, const int32_t* cand, int32_t m, float* dev, void* stream);
 
 /* HKVD top-k ("数学推导" §近似解; gradual filter of "rag的kvcache问题"
  * §渐进式过滤机制): keep the k of m candidates with the largest dev, ties to
@@ -162,7 +197,8 @@ typedef struct cb_layer_io {
   const void* k_new;     /* [n_tokens, hkv, D] recomputed keys before RoPE, by token; rows of C_l and the suffix are read */
   const void* v_new;     /* [n_tokens, hkv, D] recomputed values, by token; same rows */
   const void* q;         /* [n_tokens, hq, D] queries before RoPE, by token; rows of S_l and the suffix are read */
-  const int32_t* cand;   /* C_l, strictly ascending: NULL at layer 1 (all context tokens), else S_{l-1} */
+  const int32_t* cand;   /* C_l, strictly ascending: NULL at layer 1 (all context tokens), else S_{l-1}
+                            (CB_FILTER_RESELECT: S_1) */
   float* dev;            /* [n_cand] out at selecting layers: deviation per candidate (may be NULL otherwise) */
   int32_t* sel_tok;      /* [k] out: S_l, ascending token ids */
   int32_t* sel_row;      /* [k] out: rows of S_l in C_l */
@@ -173,7 +209,8 @@ typedef struct cb_layer_io {
 } cb_layer_io;
 
 /* One layer of the blend (1-based `layer`), all on `stream`, no host sync:
- *   selecting layers: deviation over C_l, then top-k -> S_l;
+ *   selecting layers: deviation over C_l (V or K+V, as the plan's config
+ *                     says), then top-k -> S_l;
  *   other layers:     S_l = C_l;
  *   then fused K/V for all n_tokens rows in one pass (cached rows re-rotated
  *   by their chunk offset, S_l and suffix rows encoded from k_new / v_new)
@@ -182,7 +219,8 @@ cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, vo
 
 /* All layers 1..n_layers of one request (ios[l-1] = buffers of layer l) with
  * the gradual filter wired automatically: layer l reads the candidates
- * ios[l-2].sel_tok (ios[].cand is ignored). Same results as calling
+ * ios[l-2].sel_tok (CB_FILTER_RESELECT: ios[0].sel_tok for l >= 2; ios[].cand
+ * is ignored). Same results as calling
  * cb_blend_layer for each layer in order, but scheduled over streams the plan
  * owns: every layer's deviation, top-k and fused-cache (with query encoding)
  * kernels run on one side stream, ahead of the attention, and the attention of
@@ -195,7 +233,7 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
 
 /* The stages of one layer, in the order cb_blend_layer runs them. */
 typedef enum cb_stage {
-  CB_STAGE_DEVIATION = 0, /* V deviation over C_l (selecting layers only) */
+  CB_STAGE_DEVIATION = 0, /* deviation over C_l (selecting layers only) */
   CB_STAGE_TOPK = 1,      /* top-k of the deviations -> S_l (selecting layers only) */
   CB_STAGE_FUSE = 2,      /* fused K/V for all n_tokens rows and the encoded query rows, one launch */
   CB_STAGE_ATTENTION = 3  /* HKVD attention */

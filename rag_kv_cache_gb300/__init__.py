@@ -15,7 +15,7 @@ import torch
 from . import _lib
 from ._lib import CacheBlendError, check
 
-__all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_hkvd_topk", "cb_fuse_scatter",
+__all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk", "cb_fuse_scatter",
            "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage", "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check",
            "cb_version", "LayerBuffers"]
 
@@ -46,10 +46,12 @@ class Plan:
     """A cb_plan: one blend request's shapes, RoPE table and scratch on the current device."""
 
     def __init__(self, n_chunks, chunk_len, n_suffix, hq, hkv, head_dim, rope_theta, rope_style="half",
-                 r1_pct=15, r2_pct=15):
+                 r1_pct=15, r2_pct=15, deviation="v", filter="keep"):
         lib = _lib.load()
         self.cfg = _lib.CbConfig(n_chunks, chunk_len, n_suffix, hq, hkv, head_dim, float(rope_theta),
-                                 _lib.ROPE_STYLES[rope_style], r1_pct, r2_pct)
+                                 _lib.ROPE_STYLES[rope_style], r1_pct, r2_pct, _lib.DEVIATIONS[deviation],
+                                 _lib.FILTERS[filter])
+        self.deviation, self.filter = deviation, filter
         self.n_ctx = n_chunks * chunk_len
         self.n_tokens = self.n_ctx + n_suffix
         self.hq, self.hkv, self.head_dim = hq, hkv, head_dim
@@ -57,10 +59,17 @@ class Plan:
         check(lib.cb_plan_create(ctypes.byref(self.cfg), ctypes.byref(self._h)))
 
     @classmethod
-    def from_config(cls, cfg, rope_style="half", r1_pct=None, r2_pct=None):
+    def from_config(cls, cfg, rope_style="half", r1_pct=None, r2_pct=None, deviation="v", filter="keep"):
         """From a workloads.BlendConfig (or anything with the same fields)."""
         return cls(cfg.n_chunks, cfg.chunk_len, cfg.n_suffix, cfg.hq, cfg.hkv, cfg.head_dim, cfg.rope_theta,
-                   rope_style, cfg.r1_pct if r1_pct is None else r1_pct, cfg.r2_pct if r2_pct is None else r2_pct)
+                   rope_style, cfg.r1_pct if r1_pct is None else r1_pct, cfg.r2_pct if r2_pct is None else r2_pct,
+                   deviation, filter)
+
+    def candidate_layer(self, layer):
+        """The layer whose selection is C_layer (0: all context tokens), per the plan's filter."""
+        if layer <= 1:
+            return 0
+        return 1 if self.filter == "reselect" else layer - 1
 
     @property
     def handle(self):
@@ -110,6 +119,13 @@ def cb_rope_rerotate(plan, out, x, pos_to, pos_from=None, in_rows=None, out_rows
 def cb_kv_deviation(plan, v_new, v_old, cand, m, dev, stream=None):
     check(_lib.load().cb_kv_deviation(
         plan.handle, _ptr(v_new, torch.bfloat16, "v_new"), _ptr(v_old, torch.bfloat16, "v_old"),
+        _ptr(cand, torch.int32, "cand"), m, _ptr(dev, torch.float32, "dev"), _stream(stream)))
+
+
+def cb_kv_deviation_kv(plan, k_new, k_old, v_new, v_old, cand, m, dev, stream=None):
+    check(_lib.load().cb_kv_deviation_kv(
+        plan.handle, _ptr(k_new, torch.bfloat16, "k_new"), _ptr(k_old, torch.bfloat16, "k_old"),
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(v_old, torch.bfloat16, "v_old"),
         _ptr(cand, torch.int32, "cand"), m, _ptr(dev, torch.float32, "dev"), _stream(stream)))
 
 
@@ -173,7 +189,7 @@ def _layer_io(k_old, v_old, k_new, v_new, q, cand, bufs):
 def cb_blend_request(plan, layers, stream=None):
     """All layers of one request (cb_blend_request): `layers` lists, for layers 1..n, dicts with
     k_old, v_old, k_new, v_new, q and bufs (a LayerBuffers per layer; buffers must not alias).
-    Layer l reads the candidates layers[l-2]["bufs"].sel_tok."""
+    Layer l reads the candidates layers[l-2]["bufs"].sel_tok (filter "reselect": layers[0]["bufs"].sel_tok)."""
     n = len(layers)
     arr = (_lib.CbLayerIO * n)()
     for i, L in enumerate(layers):

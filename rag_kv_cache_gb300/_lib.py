@@ -18,11 +18,13 @@ CB_OK = 0
 STATUS = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_UNSUPPORTED", 3: "CB_ERR_CUDA",
           4: "CB_ERR_TIMEOUT", 5: "CB_ERR_DEVICE_CHECK"}
 ROPE_STYLES = {"half": 0, "interleaved": 1}
+DEVIATIONS = {"v": 0, "kv": 1}  # cb_deviation
+FILTERS = {"keep": 0, "reselect": 1}  # cb_filter
 STAGES = {"deviation": 0, "topk": 1, "fuse": 2, "attention": 3}  # cb_stage
 
 # every symbol include/cacheblend.h declares
 EXPORTS = ("cb_plan_create", "cb_plan_destroy", "cb_layer_sizes", "cb_rope_rerotate", "cb_kv_deviation",
-           "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage",
+           "cb_kv_deviation_kv", "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage",
            "cb_blend_request",
            "cb_hkvd_select_noalloc", "cb_check", "cb_last_error_string", "cb_version")
 
@@ -31,7 +33,8 @@ class CbConfig(ctypes.Structure):
     _fields_ = [("n_chunks", ctypes.c_int32), ("chunk_len", ctypes.c_int32), ("n_suffix", ctypes.c_int32),
                 ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rope_theta", ctypes.c_double), ("rope_style", ctypes.c_int32),
-                ("r1_pct", ctypes.c_int32), ("r2_pct", ctypes.c_int32)]
+                ("r1_pct", ctypes.c_int32), ("r2_pct", ctypes.c_int32),
+                ("deviation", ctypes.c_int32), ("filter", ctypes.c_int32)]
 
 
 class CbLayerIO(ctypes.Structure):
@@ -65,6 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cb_layer_sizes": (i32, [vp, i32] + [ctypes.POINTER(i32)] * 4),
         "cb_rope_rerotate": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]),
         "cb_kv_deviation": (i32, [vp, vp, vp, vp, i32, vp, vp]),
+        "cb_kv_deviation_kv": (i32, [vp, vp, vp, vp, vp, vp, i32, vp, vp]),
         "cb_hkvd_topk": (i32, [vp, vp, vp, i32, i32, vp, vp, vp]),
         "cb_fuse_scatter": (i32, [vp, vp, vp, vp, vp, vp, i32, vp]),
         "cb_hkvd_attention": (i32, [vp, vp, vp, i32, vp, vp, i32, f32, vp, vp]),

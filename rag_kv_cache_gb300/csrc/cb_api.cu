@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include "../../include/cacheblend.h"
 #include "common.cuh"
@@ -105,6 +106,10 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
     return fail(CB_ERR_INVALID_ARG, "unknown rope_style %d", c.rope_style);
   if (c.r1_pct < 0 || c.r1_pct > 100 || c.r2_pct < 0 || c.r2_pct > c.r1_pct)
     return fail(CB_ERR_INVALID_ARG, "need 0 <= r2_pct <= r1_pct <= 100");
+  if (c.deviation != CB_DEV_V && c.deviation != CB_DEV_KV)
+    return fail(CB_ERR_INVALID_ARG, "unknown deviation %d", c.deviation);
+  if (c.filter != CB_FILTER_KEEP && c.filter != CB_FILTER_RESELECT)
+    return fail(CB_ERR_INVALID_ARG, "unknown filter %d", c.filter);
 
   cb_plan* p = new cb_plan();
   p->cfg = c;
@@ -123,7 +128,20 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
     const int32_t init[2] = {0, -1};
     e = cudaMemcpy(p->err, init, sizeof(init), cudaMemcpyHostToDevice);
   }
-  if (e == cudaSuccess) e = cb::launch_rope_table(p->rope_tab, p->n_tokens, c.head_dim, c.rope_theta, nullptr);
+  if (e == cudaSuccess) {
+    // (cos, sin) of p * theta^(-2j/D): the exponent (-2j)/D, theta^x, the angle and cos / sin in
+    // fp64 with the C library's routines, then rounded to fp32.
+    const int half = c.head_dim / 2;
+    std::vector<double> inv(half);
+    for (int j = 0; j < half; ++j) inv[j] = std::pow(c.rope_theta, (-2.0 * j) / c.head_dim);
+    std::vector<float2> tab((size_t)n_tokens * half);
+    for (int64_t pos = 0; pos < n_tokens; ++pos)
+      for (int j = 0; j < half; ++j) {
+        const double a = (double)pos * inv[j];
+        tab[(size_t)pos * half + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    e = cudaMemcpy(p->rope_tab, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cb_plan_destroy(p);
@@ -157,6 +175,8 @@ cb_status cb_layer_sizes(const cb_plan* plan, int32_t layer, int32_t* n_cand, in
   if (layer == 1) {
     c = plan->n_ctx, kk = k1, sel = 1;
   } else if (layer == 2) {
+    c = k1, kk = k2, sel = 1;
+  } else if (plan->cfg.filter == CB_FILTER_RESELECT) {
     c = k1, kk = k2, sel = 1;
   } else {
     c = k2, kk = k2, sel = 0;
@@ -197,9 +217,28 @@ cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, c
   CB_TRY(need_tensor(v_new, "v_new"));
   CB_TRY(need_tensor(v_old, "v_old"));
   CB_TRY(need_ptr(dev, "dev"));
-  return cuda_status(cb::launch_kv_deviation(v_new, v_old, cand, m, plan->n_ctx, plan->cfg.hkv, plan->cfg.head_dim,
-                                             dev, plan->err, static_cast<cudaStream_t>(stream)),
+  return cuda_status(cb::launch_kv_deviation(nullptr, nullptr, v_new, v_old, cand, m, plan->n_ctx, plan->cfg.hkv,
+                                             plan->cfg.head_dim, 1, 0, table(plan), dev, plan->err,
+                                             static_cast<cudaStream_t>(stream)),
                      "cb_kv_deviation");
+}
+
+cb_status cb_kv_deviation_kv(cb_plan* plan, const void* k_new, const void* k_old, const void* v_new,
+                             const void* v_old, const int32_t* cand, int32_t m, float* dev, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (m < 0) return fail(CB_ERR_INVALID_ARG, "m < 0");
+  if (m == 0) return CB_OK;
+  if (cand == nullptr && m > plan->n_ctx) return fail(CB_ERR_INVALID_ARG, "m > n_ctx without a candidate list");
+  CB_TRY(need_tensor(k_new, "k_new"));
+  CB_TRY(need_tensor(k_old, "k_old"));
+  CB_TRY(need_tensor(v_new, "v_new"));
+  CB_TRY(need_tensor(v_old, "v_old"));
+  CB_TRY(need_ptr(dev, "dev"));
+  const auto& c = plan->cfg;
+  return cuda_status(cb::launch_kv_deviation(k_new, k_old, v_new, v_old, cand, m, plan->n_ctx, c.hkv, c.head_dim,
+                                             c.chunk_len, c.rope_style, table(plan), dev, plan->err,
+                                             static_cast<cudaStream_t>(stream)),
+                     "cb_kv_deviation_kv");
 }
 
 cb_status cb_hkvd_topk(cb_plan* plan, const float* dev, const int32_t* cand, int32_t m, int32_t k,
@@ -289,11 +328,14 @@ static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* 
   if (layer == 1) cand = nullptr;
   const int32_t* sel = sh.selects ? io->sel_tok : cand;
   switch (stage) {
-    case CB_STAGE_DEVIATION:
+    case CB_STAGE_DEVIATION: {
       if (!sh.selects) return CB_OK;
-      return cuda_status(cb::launch_kv_deviation(io->v_new, io->v_old, cand, sh.n_cand, plan->n_ctx, c.hkv,
-                                                 c.head_dim, io->dev, plan->err, s),
+      const bool kv = c.deviation == CB_DEV_KV;
+      return cuda_status(cb::launch_kv_deviation(kv ? io->k_new : nullptr, kv ? io->k_old : nullptr, io->v_new,
+                                                 io->v_old, cand, sh.n_cand, plan->n_ctx, c.hkv, c.head_dim,
+                                                 c.chunk_len, c.rope_style, table(plan), io->dev, plan->err, s),
                          "deviation");
+    }
     case CB_STAGE_TOPK:
       if (!sh.selects) return CB_OK;
       return cuda_status(cb::launch_hkvd_topk(io->dev, cand, sh.n_cand, sh.k, io->sel_tok, io->sel_row, plan->err, s),
@@ -345,9 +387,14 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
   CB_TRY(check_plan(plan));
   if (n_layers < 1) return fail(CB_ERR_INVALID_ARG, "n_layers must be >= 1");
   CB_TRY(need_ptr(ios, "ios"));
+  // C_l is the selection of layer l - 1, or of layer 1 when every layer re-selects from its pool.
+  const bool reselect = plan->cfg.filter == CB_FILTER_RESELECT;
+  auto cand_of = [&](int32_t l) -> const int32_t* {
+    return l == 1 ? nullptr : ios[(reselect ? 1 : l - 1) - 1].sel_tok;
+  };
   for (int32_t l = 1; l <= n_layers; ++l) {
     LayerShape sh;
-    CB_TRY(validate_io(plan, l, &ios[l - 1], l == 1 ? nullptr : ios[l - 2].sel_tok, &sh));
+    CB_TRY(validate_io(plan, l, &ios[l - 1], cand_of(l), &sh));
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t attn_stream[2] = {s, plan->aux_attn};
@@ -356,7 +403,7 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
   CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_attn, plan->ev_fork, 0), "fork"));
   for (int32_t l = 1; l <= n_layers; ++l) {
     const cb_layer_io* io = &ios[l - 1];
-    const int32_t* cand = l == 1 ? nullptr : ios[l - 2].sel_tok;
+    const int32_t* cand = cand_of(l);
     LayerShape sh;
     CB_TRY(validate_io(plan, l, io, cand, &sh));
     for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_FUSE; ++st)

@@ -22,8 +22,6 @@ struct RopeTable {
   int32_t len;
 };
 
-cudaError_t launch_rope_table(float2* tab, int32_t len, int32_t head_dim, double theta, cudaStream_t s);
-
 // out[omap(i)] = R_{pos_to(i) - pos_from(i)} x[imap(i)], i in [0, n).
 // pos_to == nullptr: pos_to(i) = imap(i) (encode at the token's own position).
 // pos_from == nullptr: pos_from(i) = 0. pos_out (optional) receives pos_to(i).
@@ -31,8 +29,11 @@ cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap,
                              const int32_t* pos_to, int32_t* pos_out, int32_t n, int32_t n_heads,
                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s);
 
-cudaError_t launch_kv_deviation(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
-                                int32_t n_rows, int32_t hkv, int32_t head_dim, float* dev, int32_t* err,
+// Deviation per candidate in the canonical fp32 order: V only when k_new is null, else K+V
+// (the key part turned to p_old = token mod chunk_len with the table and RoPE style).
+cudaError_t launch_kv_deviation(const void* k_new, const void* k_old, const void* v_new, const void* v_old,
+                                const int32_t* cand, int32_t m, int32_t n_rows, int32_t hkv, int32_t head_dim,
+                                int32_t chunk_len, int32_t style, RopeTable t, float* dev, int32_t* err,
                                 cudaStream_t s);
 
 cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,

@@ -70,7 +70,8 @@ extern "C" cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old
   float* scratch = nullptr;
   cudaError_t e = scratch_on_current_device(&scratch);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (e == cudaSuccess) e = cb::launch_kv_deviation(v_new, v_old, cand, m, n_rows, hkv, head_dim, scratch, nullptr, s);
+  if (e == cudaSuccess) e = cb::launch_kv_deviation(nullptr, nullptr, v_new, v_old, cand, m, n_rows, hkv, head_dim, 1, 0,
+                                                       cb::RopeTable{nullptr, 0}, scratch, nullptr, s);
   if (e == cudaSuccess) e = cb::launch_hkvd_topk(scratch, cand, m, k, sel_tok, sel_row, nullptr, s);
   if (e != cudaSuccess) return noalloc_fail(CB_ERR_CUDA, cudaGetErrorString(e));
   return CB_OK;

@@ -18,21 +18,6 @@ __device__ __forceinline__ int map_row(const RowMap& m, int i) {
   return i < m.k ? (m.idx ? m.idx[i] : i) : m.base + (i - m.k);
 }
 
-// ---------------------------------------------------------------------------
-// RoPE cos/sin table: tab[p][j] = (cos a, sin a), a = p * theta^(-2j/D), fp64 then fp32.
-__global__ void rope_table_kernel(float2* tab, int len, int half, int head_dim, double log2_theta) {
-  const long long total = (long long)len * half;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(idx / half);
-    const int j = (int)(idx % half);
-    const double inv = exp2(-(2.0 * j / head_dim) * log2_theta);
-    double s, c;
-    sincos((double)p * inv, &s, &c);
-    tab[idx] = make_float2((float)c, (float)s);
-  }
-}
-
 // Rotate one row of n_heads x D bf16 by the table row `cs` (sign of sin flipped when neg).
 // One warp per row; 16-byte accesses; src may equal dst.
 template <int STYLE, int B>
@@ -217,12 +202,20 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint
 }
 
 // ---------------------------------------------------------------------------
-// V deviation, canonical order: lane l sums chunks l, l+32, ... (8 elements each)
-// as acc = fl(acc + fl(d*d)), d = fl(v_new - v_old); then a xor butterfly.
-template <int CPL>  // chunks per lane (ceil(E / 256))
-__global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* v_new, const uint8_t* v_old,
-                                                           const int32_t* cand, int m, int n_rows,
-                                                           int elems, float* dev, int32_t* err) {
+// Deviation, canonical order: lane l sums chunks l, l+32, ... (8 elements each) as
+// acc = fl(acc + fl(d*d)), then a xor butterfly over the lanes.
+//   V only (KS < 0):  d = fl(v_new - v_old).
+//   K+V (KS = RoPE style): first the key part, d = fl(x' - k_old) where x' is the recomputed
+//   key turned to the token's chunk-local position p_old = t mod chunk_len in fp32 from the
+//   table row of p_old (first pair member x' = fl(fl(x c) - fl(y s)), second member
+//   y' = fl(fl(x s) + fl(y c))); then the V part. Each lane adds all its key chunks before
+//   its V chunks. Products and sums are separately rounded (no fused multiply-add).
+template <int CPL, int KS>
+__global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* k_new, const uint8_t* k_old,
+                                                           const uint8_t* v_new, const uint8_t* v_old,
+                                                           const int32_t* cand, int m, int n_rows, int elems,
+                                                           int head_dim, int chunk_len, RopeTable tab, float* dev,
+                                                           int32_t* err) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x % kWarp;
@@ -238,6 +231,72 @@ __global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* v_new,
   }
   const int chunks = elems / 8;
   const size_t row_bytes = (size_t)elems * 2;
+  float acc = 0.0f;
+  if constexpr (KS >= 0) {
+    const uint8_t* kn = k_new + (size_t)t * row_bytes;
+    const uint8_t* ko = k_old + (size_t)t * row_bytes;
+    const float2* cs = tab.tab + (size_t)(t % chunk_len) * (head_dim / 2);
+    const int per_head = head_dim / 8;  // chunks per head
+    uint4 a[CPL], b[CPL], pa[CPL];
+#pragma unroll
+    for (int r = 0; r < CPL; ++r) {
+      const int c = lane + kWarp * r;
+      if (c < chunks) {
+        a[r] = ld_stream(kn + (size_t)c * 16);
+        b[r] = ld_stream(ko + (size_t)c * 16);
+        if (KS == 0) {  // the other members of the chunk's pairs sit D/2 elements away
+          const int ch = c % per_head;
+          pa[r] = ld_stream(kn + (size_t)(ch < per_head / 2 ? c + per_head / 2 : c - per_head / 2) * 16);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < CPL; ++r) {
+      const int c = lane + kWarp * r;
+      if (c < chunks) {
+        float x[8], o[8];
+        unpack8(a[r], x);
+        unpack8(b[r], o);
+        const int ch = c % per_head;
+        if (KS == 0) {
+          float y[8];
+          unpack8(pa[r], y);
+          const bool first = ch < per_head / 2;
+          const float4* t4 = reinterpret_cast<const float4*>(cs + (first ? ch : ch - per_head / 2) * 8);
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float4 q = __ldg(t4 + e2);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e2 + h;
+              const float c0 = h ? q.z : q.x, s0 = h ? q.w : q.y;
+              const float rot = first ? __fsub_rn(__fmul_rn(x[e], c0), __fmul_rn(y[e], s0))
+                                      : __fadd_rn(__fmul_rn(y[e], s0), __fmul_rn(x[e], c0));
+              const float d = __fsub_rn(rot, o[e]);
+              acc = __fadd_rn(acc, __fmul_rn(d, d));
+            }
+          }
+        } else {
+          const float4* t4 = reinterpret_cast<const float4*>(cs + ch * 4);
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const float4 q = __ldg(t4 + e2);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 4 * e2 + 2 * h;
+              const float c0 = h ? q.z : q.x, s0 = h ? q.w : q.y;
+              const float r0 = __fsub_rn(__fmul_rn(x[e], c0), __fmul_rn(x[e + 1], s0));
+              const float r1 = __fadd_rn(__fmul_rn(x[e], s0), __fmul_rn(x[e + 1], c0));
+              const float d0 = __fsub_rn(r0, o[e]);
+              acc = __fadd_rn(acc, __fmul_rn(d0, d0));
+              const float d1 = __fsub_rn(r1, o[e + 1]);
+              acc = __fadd_rn(acc, __fmul_rn(d1, d1));
+            }
+          }
+        }
+      }
+    }
+  }
   const uint8_t* pn = v_new + (size_t)t * row_bytes;
   const uint8_t* po = v_old + (size_t)t * row_bytes;
   uint4 a[CPL], b[CPL];
@@ -249,7 +308,6 @@ __global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* v_new,
       b[r] = ld_stream(po + (size_t)c * 16);
     }
   }
-  float acc = 0.0f;
 #pragma unroll
   for (int r = 0; r < CPL; ++r) {
     const int c = lane + kWarp * r;
@@ -538,14 +596,6 @@ int grid_for_warps(long long warps_needed, int warps_per_block) {
 
 }  // namespace
 
-cudaError_t launch_rope_table(float2* tab, int32_t len, int32_t head_dim, double theta, cudaStream_t s) {
-  const int half = head_dim / 2;
-  const long long total = (long long)len * half;
-  const int blocks = (int)((total + 255) / 256 < 152 * 8 ? (total + 255) / 256 : 152 * 8);
-  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(tab, len, half, head_dim, log2(theta));
-  return cudaPeekAtLastError();
-}
-
 cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap, const int32_t* pos_from,
                              const int32_t* pos_to, int32_t* pos_out, int32_t n, int32_t n_heads,
                              int32_t head_dim, int32_t style, RopeTable t, int32_t* err, cudaStream_t s) {
@@ -561,20 +611,42 @@ cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap,
   return cudaPeekAtLastError();
 }
 
-cudaError_t launch_kv_deviation(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
-                                int32_t n_rows, int32_t hkv, int32_t head_dim, float* dev, int32_t* err,
-                                cudaStream_t s) {
-  if (m <= 0) return cudaSuccess;
+template <int KS>
+static cudaError_t launch_kv_deviation_t(const void* k_new, const void* k_old, const void* v_new, const void* v_old,
+                                        const int32_t* cand, int32_t m, int32_t n_rows, int32_t hkv,
+                                        int32_t head_dim, int32_t chunk_len, RopeTable t, float* dev, int32_t* err,
+                                        cudaStream_t s) {
   const int elems = hkv * head_dim;
   const int cpl = (elems + 255) / 256;
   const int grid = (m + 7) / 8;
-  const uint8_t* a = (const uint8_t*)v_new;
-  const uint8_t* b = (const uint8_t*)v_old;
-  if (cpl <= 1) return launch_pdl(kv_deviation_kernel<1>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
-  if (cpl <= 2) return launch_pdl(kv_deviation_kernel<2>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
-  if (cpl <= 4) return launch_pdl(kv_deviation_kernel<4>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
-  if (cpl <= 8) return launch_pdl(kv_deviation_kernel<8>, grid, 256, 0, s, a, b, cand, m, n_rows, elems, dev, err);
+  const auto* kn = (const uint8_t*)k_new;
+  const auto* ko = (const uint8_t*)k_old;
+  const auto* vn = (const uint8_t*)v_new;
+  const auto* vo = (const uint8_t*)v_old;
+#define CB_DEV_LAUNCH(C)                                                                                      \
+  return launch_pdl(kv_deviation_kernel<C, KS>, grid, 256, 0, s, kn, ko, vn, vo, cand, m, n_rows, elems, head_dim, \
+                    chunk_len, t, dev, err)
+  if (cpl <= 1) CB_DEV_LAUNCH(1);
+  if (cpl <= 2) CB_DEV_LAUNCH(2);
+  if (cpl <= 4) CB_DEV_LAUNCH(4);
+  if (cpl <= 8) CB_DEV_LAUNCH(8);
+#undef CB_DEV_LAUNCH
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_kv_deviation(const void* k_new, const void* k_old, const void* v_new, const void* v_old,
+                                const int32_t* cand, int32_t m, int32_t n_rows, int32_t hkv, int32_t head_dim,
+                                int32_t chunk_len, int32_t style, RopeTable t, float* dev, int32_t* err,
+                                cudaStream_t s) {
+  if (m <= 0) return cudaSuccess;
+  if (k_new == nullptr)
+    return launch_kv_deviation_t<-1>(nullptr, nullptr, v_new, v_old, cand, m, n_rows, hkv, head_dim, 1, t, dev, err,
+                                     s);
+  if (style == 0)
+    return launch_kv_deviation_t<0>(k_new, k_old, v_new, v_old, cand, m, n_rows, hkv, head_dim, chunk_len, t, dev,
+                                    err, s);
+  return launch_kv_deviation_t<1>(k_new, k_old, v_new, v_old, cand, m, n_rows, hkv, head_dim, chunk_len, t, dev, err,
+                                  s);
 }
 
 cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,

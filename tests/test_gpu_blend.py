@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from conftest import assert_close_attention, assert_close_bf16
-from oracle.blend import blend_layer, gradual_filter_schedule
+from oracle.blend import blend_layer, candidate_layer, gradual_filter_schedule
 from oracle.deviation import bf16_bits_to_f64
 from workloads import get_config
 from workloads.generator import generate_layer, hkvd_noise_sets
@@ -22,17 +22,18 @@ from workloads.torch_io import bf16_bits, layer_tensors
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu_layers(cb, cfg, layers, style="half", r1=None, r2=None):
+def run_gpu_layers(cb, cfg, layers, style="half", r1=None, r2=None, deviation="v", filter="keep"):
     """Run layers 1..max(layers) on the GPU; return {layer: outputs} for the requested ones."""
-    plan = cb.Plan.from_config(cfg, rope_style=style, r1_pct=r1, r2_pct=r2)
+    plan = cb.Plan.from_config(cfg, rope_style=style, r1_pct=r1, r2_pct=r2, deviation=deviation, filter=filter)
     sets = hkvd_noise_sets(cfg)
-    bufs = [cb.LayerBuffers(plan), cb.LayerBuffers(plan)]  # ping-pong: S_{l-1} is C_l
-    cand = None
+    bufs = [cb.LayerBuffers(plan), cb.LayerBuffers(plan)]  # ping-pong
+    sels = {0: None}  # kept copies of each layer's S_l: C_l is one of them
     results = {}
     for layer in range(1, max(layers) + 1):
         inp = generate_layer(cfg, layer, sets)
         t = layer_tensors(inp)
         b = bufs[layer % 2]
+        cand = sels[plan.candidate_layer(layer)]
         cb.cb_blend_layer(plan, layer, cand=cand, bufs=b, **t)
         n_cand, k, mq, selects = plan.layer_sizes(layer)
         plan.check()
@@ -43,26 +44,26 @@ def run_gpu_layers(cb, cfg, layers, style="half", r1=None, r2=None):
                 sel_tok=b.sel_tok[:k].cpu().numpy().copy(), sel_row=b.sel_row[:k].cpu().numpy().copy(),
                 k_fused=bf16_bits(b.k_fused), v_fused=bf16_bits(b.v_fused),
                 q_rot=bf16_bits(b.q_rot[:mq]), out=bf16_bits(b.out[:mq]))
-        cand = b.sel_tok
+        sels[layer] = b.sel_tok[:k].clone()
     plan.close()
     return results
 
 
-def oracle_layers(cfg, layers, style="half", attention_rows=None):
+def oracle_layers(cfg, layers, style="half", attention_rows=None, deviation="v", filter="keep"):
     """The oracle's blend for the requested layers (selection chain followed from layer 1)."""
     sets = hkvd_noise_sets(cfg)
-    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct)
-    cand = np.arange(cfg.n_ctx)
+    sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct, filter)
+    sels = {0: np.arange(cfg.n_ctx)}
     out = {}
     for layer, k, selects in sched[: max(layers)]:
         inp = generate_layer(cfg, layer, sets)
         want = layer in layers
         rows = attention_rows(k + cfg.n_suffix, layer) if (want and attention_rows) else None
-        res = blend_layer(cfg, inp, layer, cand, k, selects, style,
-                          attention_rows=(rows if want else False))
+        res = blend_layer(cfg, inp, layer, sels[candidate_layer(layer, filter)], k, selects, style,
+                          attention_rows=(rows if want else False), deviation=deviation)
         if want:
             out[layer] = res
-        cand = res.sel_tok
+        sels[layer] = res.sel_tok
     return out
 
 
@@ -101,6 +102,19 @@ def test_small_multilayer_gradual_filter(cb):
     assert np.array_equal(g[4]["sel_tok"], g[2]["sel_tok"])
 
 
+@pytest.mark.parametrize("deviation,filter,style", [("kv", "keep", "half"), ("kv", "keep", "interleaved"),
+                                                   ("v", "reselect", "half"), ("kv", "reselect", "interleaved")])
+def test_small_multilayer_variants(cb, deviation, filter, style):
+    # the K+V deviation and the per-layer re-selection reading of the gradual filter
+    cfg = dataclasses.replace(get_config("mistral7b"), name="small5", config_id=91, n_chunks=5, chunk_len=96,
+                              n_suffix=24, layers=5)
+    g = run_gpu_layers(cb, cfg, [1, 2, 3, 4, 5], style, deviation=deviation, filter=filter)
+    o = oracle_layers(cfg, [1, 2, 3, 4, 5], style, deviation=deviation, filter=filter)
+    for layer in range(1, 6):
+        assert o[layer].dev is not None or filter == "keep"
+        compare(g[layer], o[layer], cfg)
+
+
 @pytest.mark.parametrize("r", [5, 10, 15, 30, 50, 100])
 def test_ratio_sweep(cb, r):
     cfg = get_config("sweep").with_ratio(r)
@@ -128,20 +142,31 @@ def test_full_size_workloads(cb, name, layers):
         compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])))
 
 
-@pytest.mark.parametrize("name,layers", [("mistral7b", 4), ("tiny", 1)])
-def test_request_scheduling_matches_layer_by_layer(cb, name, layers):
+def test_full_size_kv_reselect(cb):
+    # Mistral-7B-shaped, layers 1-4 with the K+V deviation and re-selection at every layer
+    cfg = get_config("mistral7b")
+    rng = np.random.default_rng(77)
+    pick = lambda mq, layer: np.unique(np.concatenate([[0, mq - 1], rng.choice(mq, size=48, replace=False)]))
+    g = run_gpu_layers(cb, cfg, [1, 2, 3, 4], deviation="kv", filter="reselect")
+    o = oracle_layers(cfg, [1, 2, 3, 4], attention_rows=pick, deviation="kv", filter="reselect")
+    for layer in (1, 2, 3, 4):
+        compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])))
+
+
+@pytest.mark.parametrize("name,layers,deviation,filter", [("mistral7b", 4, "v", "keep"), ("tiny", 1, "v", "keep"),
+                                                          ("mistral7b", 4, "kv", "reselect")])
+def test_request_scheduling_matches_layer_by_layer(cb, name, layers, deviation, filter):
     # cb_blend_request overlaps layers on several streams; its outputs must be the same bytes
     # as calling cb_blend_layer layer after layer.
     cfg = get_config(name)
-    plan = cb.Plan.from_config(cfg)
+    plan = cb.Plan.from_config(cfg, deviation=deviation, filter=filter)
     sets = hkvd_noise_sets(cfg)
     ins = [layer_tensors(generate_layer(cfg, layer, sets)) for layer in range(1, layers + 1)]
     seq = [cb.LayerBuffers(plan) for _ in range(layers)]
     req = [cb.LayerBuffers(plan) for _ in range(layers)]
-    cand = None
     for li in range(layers):
-        cb.cb_blend_layer(plan, li + 1, cand=cand, bufs=seq[li], **ins[li])
-        cand = seq[li].sel_tok
+        c = plan.candidate_layer(li + 1)
+        cb.cb_blend_layer(plan, li + 1, cand=None if c == 0 else seq[c - 1].sel_tok, bufs=seq[li], **ins[li])
     for _ in range(2):  # twice: the second call reuses the plan's streams and events
         cb.cb_blend_request(plan, [dict(bufs=req[li], **ins[li]) for li in range(layers)])
     torch.cuda.synchronize()

@@ -13,7 +13,7 @@ import torch
 
 from conftest import assert_close_bf16
 from oracle.attention import causal_gqa_attention
-from oracle.deviation import bf16_bits_to_f64, deviation_canonical_f32
+from oracle.deviation import bf16_bits_to_f64, deviation_canonical_f32, kv_deviation_canonical_f32
 from oracle.rope import rerotate, rope_rotate, round_bf16
 from oracle.topk import hkvd_topk
 from workloads import get_config
@@ -135,6 +135,43 @@ def test_deviation_bit_exact(cb, hkv, d):
     ref_all = deviation_canonical_f32(v_new[:n_ctx], v_old)
     assert np.array_equal(dev_all.cpu().numpy().view(np.uint32), ref_all.view(np.uint32))
     assert dev_all[5].item() == 0.0
+
+
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+@pytest.mark.parametrize("hkv,d", [(2, 64), (8, 128), (16, 128), (3, 64)])
+def test_kv_deviation_bit_exact(cb, hkv, d, style):
+    # K+V deviation: the recomputed key turned to p_old = t mod chunk_len (chunk_len 333, so the
+    # table rows differ from the token ids) in fp32 from the plan's table, then the canonical sum.
+    cfg = dataclasses.replace(get_config("tiny"), hkv=hkv, hq=hkv * 2, head_dim=d, n_chunks=4, chunk_len=333)
+    plan = _plan(cb, cfg, style)
+    rng = np.random.default_rng(hkv * 100 + d + (style == "half"))
+    n_ctx, n = cfg.n_ctx, cfg.n_tokens
+    draw = lambda rows, sc=1.0: f32_to_bf16_bits((sc * rng.standard_normal((rows, hkv, d))).astype(np.float32))
+    k_old, v_old = draw(n_ctx), draw(n_ctx)
+    scale = np.exp(rng.uniform(-9, 1, size=(n, 1, 1))).astype(np.float32)
+    k_new = f32_to_bf16_bits(np.concatenate([(k_old.astype(np.uint32) << 16).view(np.float32),
+                                             np.zeros((cfg.n_suffix, hkv, d), np.float32)])
+                             + scale * rng.standard_normal((n, hkv, d)).astype(np.float32))
+    v_new = draw(n)
+    v_new[7] = v_old[7]
+    cand = np.sort(rng.choice(n_ctx, size=n_ctx // 3, replace=False))
+    dev = torch.empty(cand.size, dtype=torch.float32, device="cuda")
+    cb.cb_kv_deviation_kv(plan, bf16_tensor(k_new), bf16_tensor(k_old), bf16_tensor(v_new), bf16_tensor(v_old),
+                          _i32(cand), cand.size, dev)
+    plan.check()
+    ref = kv_deviation_canonical_f32(k_new[cand], k_old[cand], v_new[cand], v_old[cand], cand % cfg.chunk_len,
+                                     cfg.rope_theta, style)
+    assert np.array_equal(dev.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # identity candidate list, and a token whose key part is exactly zero (p_old = 0, same key)
+    k_new[0] = k_old[0]
+    dev_all = torch.empty(n_ctx, dtype=torch.float32, device="cuda")
+    cb.cb_kv_deviation_kv(plan, bf16_tensor(k_new), bf16_tensor(k_old), bf16_tensor(v_new), bf16_tensor(v_old),
+                          None, n_ctx, dev_all)
+    plan.check()
+    ref_all = kv_deviation_canonical_f32(k_new[:n_ctx], k_old, v_new[:n_ctx], v_old,
+                                         np.arange(n_ctx) % cfg.chunk_len, cfg.rope_theta, style)
+    assert np.array_equal(dev_all.cpu().numpy().view(np.uint32), ref_all.view(np.uint32))
+    assert dev_all[0].item() == float(deviation_canonical_f32(v_new[:1], v_old[:1])[0])
 
 
 def test_deviation_golden_rounding_cases(cb):
