@@ -55,3 +55,21 @@ def causal_gqa_attention(q, q_pos, k, v, scale: float | None = None, block: int 
             if return_vscale:
                 vscale[b0:b1, h, :] = p @ np.abs(v[:kend, g, :])
     return (out, vscale) if return_vscale else out
+
+
+def decode_attention(q, k, v, scale: float | None = None, return_vscale: bool = False):
+    """One decode step ("rag的kvcache问题" §阶段 2 (Decode)): the newest token is the only query.
+
+    Its query row q [Hq, D] (RoPE-encoded at its position n_keys - 1) attends over the whole
+    cache k, v [n_keys, Hkv, D], whose last row is the newest token's own key and value, so
+    no key is masked: O[h] = sum_{j < n_keys} softmax_j(q[h] . k[j, g] * scale) v[j, g].
+    This is the causal attention above for the single row at position n_keys - 1.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n = np.asarray(k).shape[0]
+    if n < 1:
+        raise ValueError("decode needs at least the newest token's own key")
+    res = causal_gqa_attention(q[None], np.array([n - 1]), k, v, scale=scale, return_vscale=return_vscale)
+    if return_vscale:
+        return res[0][0], res[1][0]
+    return res[0]

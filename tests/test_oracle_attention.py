@@ -67,3 +67,32 @@ def test_weights_sum_to_one():
     k = rng.standard_normal((90, 2, 16))
     o = causal_gqa_attention(q, np.sort(rng.choice(90, 20, replace=False)), k, np.ones((90, 2, 16)))
     np.testing.assert_allclose(o, 1.0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- decode ("rag的kvcache问题" §阶段 2)
+from oracle.attention import decode_attention  # noqa: E402
+
+
+@pytest.mark.parametrize("hq,hkv,d,n", [(4, 2, 64, 300), (8, 1, 16, 77), (16, 2, 128, 260)])
+def test_decode_is_the_last_row_of_library_causal_attention(hq, hkv, d, n):
+    rng = np.random.default_rng(hq + n)
+    q = rng.standard_normal((n, hq, d))
+    k = rng.standard_normal((n, hkv, d))
+    v = rng.standard_normal((n, hkv, d))
+    got = decode_attention(q[-1], k, v)
+    np.testing.assert_allclose(got, _sdpa_causal(q, k, v)[-1], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_with_one_key_returns_its_value():
+    rng = np.random.default_rng(5)
+    q, k, v = rng.standard_normal((8, 64)), rng.standard_normal((1, 2, 64)), rng.standard_normal((1, 2, 64))
+    got = decode_attention(q, k, v)
+    np.testing.assert_array_equal(got, np.repeat(v[0], 4, axis=0))
+
+
+def test_decode_zero_query_averages_all_values():
+    # q = 0 gives equal scores: every key weighs 1/n (nothing is masked in decode)
+    rng = np.random.default_rng(6)
+    k, v = rng.standard_normal((2, 37, 2, 32))
+    got = decode_attention(np.zeros((4, 32)), k, v)
+    np.testing.assert_allclose(got, np.repeat(v.mean(axis=0), 2, axis=0), rtol=1e-13)
