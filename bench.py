@@ -59,6 +59,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--path", choices=["blend", "decode"], default="blend",
+                    help="blend: the per-layer blend (default); decode: one decode step's attention over "
+                         "every layer's cache after the request")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (smaller captures for profiling; not a bench line)")
     ap.add_argument("--deviation", choices=["v", "kv"], default="v",
                     help="rank by the V deviation (default) or by the K+V deviation")
     ap.add_argument("--filter", choices=["keep", "reselect"], default="keep",
@@ -437,6 +442,91 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_decode(args, cfg):
+    """Decode path: per step, the newest token's attention over each layer's cache (n_tokens + 1 keys)."""
+    import torch
+    import torch.distributed as dist
+
+    import rag_kv_cache_gb300 as cb
+    from rag_kv_cache_gb300.build import build
+    from workloads.generator import generate_decode
+    from workloads.torch_io import bf16_tensor
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    ins = [generate_decode(cfg, layer) for layer in range(1, cfg.layers + 1)]
+    n_keys = cfg.n_tokens + 1
+    d_k = [bf16_tensor(x.k, dev) for x in ins]
+    d_v = [bf16_tensor(x.v, dev) for x in ins]
+    d_q = [bf16_tensor(x.q, dev) for x in ins]
+    outs = [torch.empty((cfg.hq, cfg.head_dim), dtype=torch.bfloat16, device=dev) for _ in ins]
+    plan = cb.Plan.from_config(cfg)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for li in range(cfg.layers):
+            cb.cb_decode_attention(plan, d_q[li], d_k[li], d_v[li], n_keys, outs[li], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    plan.check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clocks:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            stop.record(stream)
+        stream.synchronize()
+    ms = start.elapsed_time(stop)
+    plan.check()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    row_kv = cfg.hkv * cfg.head_dim * 2
+    bytes_launch = 2.0 * n_keys * row_kv + 2.0 * cfg.hq * cfg.head_dim * 2
+    us_launch = 1e3 * ms_step / cfg.layers
+    gbs = bytes_launch / (us_launch * 1e-6) / 1e9
+    peaks = load_peaks()
+    line = {"metric": "decode steps/s (one new token, attention of every layer)", "value": world * 1e3 / ms_step,
+            "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1) bf16 caches and queries",
+            "config": {"workload": workload_desc(cfg), "path": "decode", "n_keys": n_keys,
+                       "l2": f"inputs larger than L2: {cfg.layers * bytes_launch / 1e9:.2f} GB per step",
+                       "cuda_graph": True},
+            "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"{peaks['source']} copy bandwidth", "bytes_per_launch": bytes_launch,
+                         "launches_per_step": cfg.layers, "avg_launch_us": us_launch},
+            "gpu_launches": cfg.layers * args.steps, "clocks": clocks.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
     """Metric through the C ABI with host buffers: H2D of every layer's inputs and D2H of its outputs timed."""
     import torch
@@ -514,8 +604,14 @@ def main():
     from workloads import get_config
 
     cfg = get_config(args.workload)
+    if args.layers is not None:
+        import dataclasses
+
+        cfg = dataclasses.replace(cfg, layers=max(1, min(cfg.layers, args.layers)))
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.path == "decode":
+        return run_decode(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -190,6 +190,20 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                             const void* k, const void* v, int32_t n_keys, float scale, void* out,
                             void* stream);
 
+/* Decode attention over a cache ("rag的kvcache问题" §阶段 2 (Decode): after the prefill the
+ * newest token is the only query, and its [1, d] query row is matched against the whole
+ * cached K/V, which makes the step memory-bound). For the newest token at position
+ * n_keys - 1, with its own key and value already in the cache's last row:
+ *   out[h] = sum_{j < n_keys} softmax_j(scale * q[h] . k[j, g]) v[j, g],  g = h / (hq/hkv),
+ * q, out: [hq, D] (q RoPE-encoded at n_keys - 1); k, v: [n_keys, hkv, D], key j at
+ * position j (e.g. a layer's k_fused / v_fused with the new token appended). scale <= 0
+ * selects 1/sqrt(D). fp32 dot products and softmax on the CUDA cores, bf16 output. The keys
+ * of each kv head are split over up to 40 CTAs whose partial results meet in the plan's
+ * decode scratch (the last CTA of a kv head merges them), so decode calls on one plan must
+ * not overlap on the GPU: order them on one stream, or give each stream its own plan. */
+cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
+                              float scale, void* out, void* stream);
+
 /* Buffers of one layer for cb_blend_layer. Sizes from cb_layer_sizes. */
 typedef struct cb_layer_io {
   const void* k_old;     /* [n_ctx, hkv, D] cached keys, at chunk-local positions */

@@ -15,9 +15,9 @@ import torch
 from . import _lib
 from ._lib import CacheBlendError, check
 
-__all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk", "cb_fuse_scatter",
-           "cb_hkvd_attention", "cb_blend_layer", "cb_blend_stage", "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check",
-           "cb_version", "LayerBuffers"]
+__all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk",
+           "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_blend_layer", "cb_blend_stage",
+           "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check", "cb_version", "LayerBuffers"]
 
 
 def _ptr(t, dtype=None, name="tensor"):
@@ -147,6 +147,13 @@ def cb_hkvd_attention(plan, q, q_pos, mq, k, v, n_keys, out, scale=0.0, stream=N
         plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(q_pos, torch.int32, "q_pos"), mq,
         _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"), n_keys, float(scale),
         _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def cb_decode_attention(plan, q, k, v, n_keys, out, scale=0.0, stream=None):
+    """One decode step's attention: q [Hq, D] at position n_keys - 1 over k, v [>= n_keys, Hkv, D]."""
+    check(_lib.load().cb_decode_attention(
+        plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        n_keys, float(scale), _ptr(out, torch.bfloat16, "out"), _stream(stream)))
 
 
 def cb_hkvd_select_noalloc(v_new, v_old, cand, m, k, n_rows, sel_tok, sel_row, stream=None):

@@ -22,6 +22,7 @@ struct cb_plan {
   cudaStream_t aux_stream;  // cb_blend_request: every layer's deviation, top-k and fuse (with the query encoding)
   cudaStream_t aux_attn;    // cb_blend_request: attention of even layers (odd layers on the caller's stream)
   cudaEvent_t ev_fork, ev_ready, ev_join;
+  cb::DecodeScratch decode;  // cb_decode_attention's split partials and ticket counters
 };
 
 namespace {
@@ -123,6 +124,16 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    p->decode.target_ctas = 2 * (sms > 0 ? sms : 1);
+  }
+  const size_t dec_units = (size_t)c.hq * cb::decode_max_splits();  // (kv head, split, q head) triples
+  if (e == cudaSuccess) e = cudaMalloc(&p->decode.part_o, sizeof(float) * dec_units * c.head_dim);
+  if (e == cudaSuccess) e = cudaMalloc(&p->decode.part_ml, sizeof(float2) * dec_units);
+  if (e == cudaSuccess) e = cudaMalloc(&p->decode.tickets, sizeof(int32_t) * c.hkv);
+  if (e == cudaSuccess) e = cudaMemset(p->decode.tickets, 0, sizeof(int32_t) * c.hkv);
 
   if (e == cudaSuccess) {
     const int32_t init[2] = {0, -1};
@@ -156,6 +167,9 @@ cb_status cb_plan_destroy(cb_plan* plan) {
   cudaDeviceSynchronize();
   cudaFree(plan->rope_tab);
   cudaFree(plan->err);
+  cudaFree(plan->decode.part_o);
+  cudaFree(plan->decode.part_ml);
+  cudaFree(plan->decode.tickets);
   if (plan->aux_stream) cudaStreamDestroy(plan->aux_stream);
   if (plan->aux_attn) cudaStreamDestroy(plan->aux_attn);
   if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
@@ -288,6 +302,22 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                                                plan->cfg.head_dim, scale, out, plan->err,
                                                static_cast<cudaStream_t>(stream)),
                      "cb_hkvd_attention");
+}
+
+cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
+                              float scale, void* out, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (n_keys < 0) return fail(CB_ERR_INVALID_ARG, "n_keys < 0");
+  if (n_keys == 0) return CB_OK;
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  CB_TRY(need_tensor(out, "out"));
+  const auto& c = plan->cfg;
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)c.head_dim);
+  return cuda_status(cb::launch_decode_attention(q, k, v, n_keys, c.hq, c.hkv, c.head_dim, scale, out, plan->decode,
+                                                 static_cast<cudaStream_t>(stream)),
+                     "cb_decode_attention");
 }
 
 struct LayerShape {

@@ -73,4 +73,21 @@ cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, 
                                   const void* v, int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim,
                                   float scale, void* out, int32_t* err, cudaStream_t s);
 
+// Scratch of the decode attention (owned by the plan): per (kv head, split, q head) an
+// unnormalised output row and its (max, sum), and one ticket counter per kv head that is
+// zero between calls (the kernel leaves it zero).
+struct DecodeScratch {
+  float* part_o;      // [hkv][decode_max_splits()][G][D]
+  float2* part_ml;    // [hkv][decode_max_splits()][G]
+  int32_t* tickets;   // [hkv]
+  int32_t target_ctas;  // CTAs to aim for over all kv heads (two per SM)
+};
+
+int32_t decode_max_splits();
+
+// Decode attention: one query row q [hq, D] over the whole cache k, v [n_keys, hkv, D].
+cudaError_t launch_decode_attention(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq,
+                                    int32_t hkv, int32_t head_dim, float scale, void* out, const DecodeScratch& ws,
+                                    cudaStream_t s);
+
 }  // namespace cb

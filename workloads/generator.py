@@ -27,6 +27,7 @@ from .configs import BlendConfig
 
 _T_K_OLD, _T_V_OLD, _T_K_EPS, _T_V_EPS, _T_Q = 0, 1, 2, 3, 4
 _T_K_SUF, _T_V_SUF, _T_LOGN, _T_SETS = 5, 6, 7, 100
+_T_DEC_K, _T_DEC_V, _T_DEC_Q = 200, 201, 202
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -119,3 +120,20 @@ def generate_layer(cfg: BlendConfig, layer: int, sets: list | None = None) -> La
 
     q = f32_to_bf16_bits(_rng(cfg, layer, _T_Q).standard_normal((n, hq, d), dtype=np.float32))
     return LayerInputs(layer, k_old, v_old, k_new, v_new, q, s[:, 0, 0].copy(), hset)
+
+
+@dataclass
+class DecodeInputs:
+    layer: int
+    k: np.ndarray  # uint16 bf16 bits [n_keys, hkv, d]: the layer's cache after the request, plus one token
+    v: np.ndarray  # uint16 bf16 bits [n_keys, hkv, d]
+    q: np.ndarray  # uint16 bf16 bits [hq, d]: the newest token's query (taken as already encoded)
+
+
+def generate_decode(cfg: BlendConfig, layer: int, extra: int = 1) -> DecodeInputs:
+    """One decode step's inputs for a layer: N(0, 1) caches of n_tokens + extra rows and a query."""
+    n = cfg.n_tokens + extra
+    k = f32_to_bf16_bits(_rng(cfg, layer, _T_DEC_K).standard_normal((n, cfg.hkv, cfg.head_dim), dtype=np.float32))
+    v = f32_to_bf16_bits(_rng(cfg, layer, _T_DEC_V).standard_normal((n, cfg.hkv, cfg.head_dim), dtype=np.float32))
+    q = f32_to_bf16_bits(_rng(cfg, layer, _T_DEC_Q).standard_normal((cfg.hq, cfg.head_dim), dtype=np.float32))
+    return DecodeInputs(layer, k, v, q)
