@@ -25,6 +25,10 @@ Parity status per function:
   attention.causal_gqa_attention       pinned (library causal attention, single key, equal scores)
   blend.gradual_filter_schedule        parity unpinned beyond structure (the pages fix no
                                        worked example of the schedule)
+  deviation.kv_deviation_canonical_f32 pinned (closed form, frame invariance, plain loops, bound)
+  attention.decode_attention           pinned (last row of library causal attention, special cases)
+  diagnostics.attention_deviation      pinned (definition, r = 100% gives exactly 0)
+  diagnostics.attention_sparsity       pinned (closed form for equal scores, library softmax matrix)
 """
 
-from . import attention, blend, deviation, fuse, positions, rope, topk  # noqa: F401
+from . import attention, blend, deviation, diagnostics, fuse, positions, rope, topk  # noqa: F401
