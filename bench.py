@@ -59,9 +59,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--path", choices=["blend", "decode"], default="blend",
+    ap.add_argument("--path", choices=["blend", "decode", "diagnostics"], default="blend",
                     help="blend: the per-layer blend (default); decode: one decode step's attention over "
-                         "every layer's cache after the request")
+                         "every layer's cache after the request; diagnostics: attention deviation of the "
+                         "fused cache from a full prefill over the recompute ratios, and attention sparsity")
+    ap.add_argument("--eps", type=float, default=1e-3, help="sparsity threshold of the diagnostics path")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller captures for profiling; not a bench line)")
     ap.add_argument("--deviation", choices=["v", "kv"], default="v",
@@ -527,6 +529,116 @@ def run_decode(args, cfg):
     return 0
 
 
+def run_diagnostics(args, cfg):
+    """Diagnostics path on one layer: for every recompute ratio of the workload's sweep (else r1),
+    blend the layer and measure ||Attn(Q, K_fused, V_fused) - Attn(Q, K_new, V_new)|| over all
+    query rows against a full prefill, and the full prefill's Sparsity(A, eps). Times the
+    diagnostics of one ratio: both encodes, the fused-cache attention, the two passes of the
+    sparsity count and the reductions."""
+    import dataclasses
+
+    import torch
+
+    import rag_kv_cache_gb300 as cb
+    from rag_kv_cache_gb300.build import build
+    from workloads.generator import generate_layer
+    from workloads.torch_io import layer_tensors
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    ratios = list(cfg.sweep_pct) or [cfg.r1_pct]
+    inp = generate_layer(cfg, 1)
+    t = layer_tensors(inp, dev)
+    n, hq, d = cfg.n_tokens, cfg.hq, cfg.head_dim
+    pos = torch.arange(n, dtype=torch.int32, device=dev)
+    k_full = torch.empty((n, cfg.hkv, d), dtype=torch.bfloat16, device=dev)
+    q_all = torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev)
+    o_full, o_fused = torch.empty_like(q_all), torch.empty_like(q_all)
+    stats = torch.empty((n, hq, 2), dtype=torch.float32, device=dev)
+    counts = torch.empty((n, hq), dtype=torch.int32, device=dev)
+    total = torch.empty(1, dtype=torch.int64, device=dev)
+    sums = torch.empty(2, dtype=torch.float64, device=dev)
+    stream = torch.cuda.Stream(dev)
+    series, timed_plan = {}, None
+    for r in ratios:
+        plan = cb.Plan.from_config(dataclasses.replace(cfg, r1_pct=r, r2_pct=r))
+        bufs = cb.LayerBuffers(plan, dev)
+
+        def diag(plan=plan, bufs=bufs):
+            cb.cb_rope_rerotate(plan, k_full, t["k_new"], pos, stream=stream)
+            cb.cb_rope_rerotate(plan, q_all, t["q"], pos, stream=stream)
+            cb.cb_hkvd_attention(plan, q_all, pos, n, bufs.k_fused, bufs.v_fused, n, o_fused, stream=stream)
+            cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_full, stats, counts,
+                                     total, stream=stream)
+            cb.cb_output_deviation(plan, o_fused, o_full, n, sums, stream=stream)
+
+        with torch.cuda.stream(stream):
+            cb.cb_blend_layer(plan, 1, cand=None, bufs=bufs, stream=stream, **t)
+            diag()
+        stream.synchronize()
+        plan.check()
+        s2 = sums.cpu().numpy()
+        series[str(r)] = {"dev": float(np.sqrt(s2[0])), "ref": float(np.sqrt(s2[1])),
+                          "rel": float(np.sqrt(s2[0] / s2[1]))}
+        sparsity = int(total.item()) / float(hq * n * n)
+        if r == ratios[-1]:
+            timed_plan = plan
+            # time the diagnostics of this ratio, and the counting pass alone
+            for _ in range(args.warmup):
+                with torch.cuda.stream(stream):
+                    diag()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                diag()
+            gc = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gc, stream=stream):
+                cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_full, stats,
+                                         counts, total, stream=stream)
+            start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]
+            with ClockSampler(gpu_index) as clocks:
+                with torch.cuda.stream(stream):
+                    start.record(stream)
+                    for _ in range(args.steps):
+                        g.replay()
+                    stop.record(stream)
+                stream.synchronize()
+                ms = start.elapsed_time(stop) / args.steps
+                with torch.cuda.stream(stream):
+                    start.record(stream)
+                    for _ in range(args.steps):
+                        gc.replay()
+                    stop.record(stream)
+                stream.synchronize()
+                ms_count = start.elapsed_time(stop) / args.steps
+        else:
+            plan.close()
+    timed_plan.check()
+    flops = 4.0 * hq * d * n * (n + 1) / 2.0  # one causal attention over all n rows
+    peaks = load_peaks()
+    achieved = 2 * flops / (ms_count * 1e-3) / 1e12  # the sparsity count runs the attention twice
+    line = {"metric": "diagnostics time per layer (deviation over all rows + sparsity)", "value": ms,
+            "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": data_desc(cfg),
+            "config": {"workload": workload_desc(cfg), "path": "diagnostics", "n_tokens": n, "eps": args.eps,
+                       "timed_ratio_pct": ratios[-1], "cuda_graph": True},
+            "deviation_vs_r": series, "sparsity": sparsity,
+            "roofline": {"kernel": "hkvd_attention (statistics and counting passes)", "bound": "tensor",
+                         "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 sustained", "ms_sparsity_count": ms_count},
+            "gpu_launches": 8 * args.steps, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    timed_plan.close()
+    return 0
+
+
 def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
     """Metric through the C ABI with host buffers: H2D of every layer's inputs and D2H of its outputs timed."""
     import torch
@@ -612,6 +724,8 @@ def main():
         return run_reference(args, cfg)
     if args.path == "decode":
         return run_decode(args, cfg)
+    if args.path == "diagnostics":
+        return run_diagnostics(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -204,6 +204,29 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
 cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
                               float scale, void* out, void* stream);
 
+/* Attention sparsity ("数学推导" §注意力稀疏性的量化分析: Sparsity(A, eps) =
+ * |{(i, j): A_ij < eps}| / n^2 for the attention weights A): for the causal attention of
+ * cb_hkvd_attention (same q, q_pos, k, v, n_keys, scale; masked keys have weight 0 and count),
+ * counts the weights below eps of every query row and head over all n_keys keys:
+ *   counts[i * hq + h] = |{j < n_keys: A[h]_ij < eps}|,  *total = sum of counts (uint64).
+ * Two launches of the attention kernel: the first writes out (as cb_hkvd_attention) and
+ * row_stats ([mq, hq] float2, the softmax's (max, sum) in log2 units), the second recomputes the
+ * same scores and compares them with max + log2(eps * sum); then a reduction writes *total.
+ * Sparsity = total / (hq * mq * n_keys) (with q_pos = 0 .. n - 1 and n_keys = n this is the
+ * page's n x n figure summed over heads). eps must be positive. Weights within about 1e-5 of eps
+ * (relative) may fall on either side of it (fp32 scores and softmax sums). */
+cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
+                                const void* v, int32_t n_keys, float scale, float eps, void* out, void* row_stats,
+                                int32_t* counts, uint64_t* total, void* stream);
+
+/* Attention deviation ("数学推导" §形式化: ||Attention(Q, K_fused, V_fused) -
+ * Attention(Q, K_new, V_new)||, the objective the HKVD selection approximates): over `rows`
+ * rows of [hq, D] bf16 outputs, sums[0] = sum (o - o_ref)^2 and sums[1] = sum o_ref^2 in fp64
+ * (device memory, overwritten). The Frobenius norms are their square roots. The blocks' partial
+ * sums are added in no fixed order, so the last bits can differ between runs. */
+cb_status cb_output_deviation(cb_plan* plan, const void* o, const void* o_ref, int32_t rows, double* sums,
+                              void* stream);
+
 /* Buffers of one layer for cb_blend_layer. Sizes from cb_layer_sizes. */
 typedef struct cb_layer_io {
   const void* k_old;     /* [n_ctx, hkv, D] cached keys, at chunk-local positions */

@@ -46,12 +46,13 @@ def attention_deviation(o, o_ref):
     return float(np.sqrt(np.sum((o - o_ref) ** 2))), float(np.sqrt(np.sum(o_ref ** 2)))
 
 
-def attention_sparsity(q, q_pos, k, eps: float, scale: float | None = None, band: float = 1e-3):
+def attention_sparsity(q, q_pos, k, eps: float, scale: float | None = None, band: float = 1e-3,
+                       per_row: bool = False):
     """Count of causal attention weights below eps over rows q_pos and keys 0..n_keys-1.
 
     q [mq, Hq, D] (encoded), k [n_keys, Hkv, D]. Returns (count, near, total): count of
     entries A_ij < eps (masked entries are 0), entries with |A_ij - eps| <= band * eps,
-    and total = Hq * mq * n_keys.
+    and total = Hq * mq * n_keys; with per_row, also the [mq, Hq] arrays of both counts.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -62,16 +63,18 @@ def attention_sparsity(q, q_pos, k, eps: float, scale: float | None = None, band
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     visible = np.arange(n)[None, :] <= q_pos[:, None]
-    count = near = 0
+    rows_count = np.zeros((mq, hq), dtype=np.int64)
+    rows_near = np.zeros((mq, hq), dtype=np.int64)
     for h in range(hq):
         s = (q[:, h, :] @ k[:, h // group, :].T) * scale
         s = np.where(visible, s, -np.inf)
         s = s - s.max(axis=1, keepdims=True)
         a = np.exp(s)
         a = a / a.sum(axis=1, keepdims=True)
-        count += int(np.sum(a < eps))
-        near += int(np.sum(np.abs(a - eps) <= band * eps))
-    return count, near, hq * mq * n
+        rows_count[:, h] = np.sum(a < eps, axis=1)
+        rows_near[:, h] = np.sum(np.abs(a - eps) <= band * eps, axis=1)
+    out = (int(rows_count.sum()), int(rows_near.sum()), hq * mq * n)
+    return out + (rows_count, rows_near) if per_row else out
 
 
 def blend_diagnostics(cfg, inp, res, eps: float, style: str = "half"):

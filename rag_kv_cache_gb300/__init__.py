@@ -16,7 +16,8 @@ from . import _lib
 from ._lib import CacheBlendError, check
 
 __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk",
-           "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_blend_layer", "cb_blend_stage",
+           "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_attention_sparsity",
+           "cb_output_deviation", "cb_blend_layer", "cb_blend_stage",
            "cb_blend_request", "cb_hkvd_select_noalloc", "cb_check", "cb_version", "LayerBuffers"]
 
 
@@ -154,6 +155,24 @@ def cb_decode_attention(plan, q, k, v, n_keys, out, scale=0.0, stream=None):
     check(_lib.load().cb_decode_attention(
         plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
         n_keys, float(scale), _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def cb_attention_sparsity(plan, q, q_pos, mq, k, v, n_keys, eps, out, row_stats, counts, total, scale=0.0,
+                          stream=None):
+    """Counts of attention weights below eps (see cacheblend.h); row_stats float32 [mq, hq, 2],
+    counts int32 [mq, hq], total int64 [1] (device, written as an unsigned count)."""
+    check(_lib.load().cb_attention_sparsity(
+        plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(q_pos, torch.int32, "q_pos"), mq,
+        _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"), n_keys, float(scale), float(eps),
+        _ptr(out, torch.bfloat16, "out"), _ptr(row_stats, torch.float32, "row_stats"),
+        _ptr(counts, torch.int32, "counts"), _ptr(total, torch.int64, "total"), _stream(stream)))
+
+
+def cb_output_deviation(plan, o, o_ref, rows, sums, stream=None):
+    """sums (float64 [2], device) = (sum (o - o_ref)^2, sum o_ref^2) over rows x hq x D."""
+    check(_lib.load().cb_output_deviation(
+        plan.handle, _ptr(o, torch.bfloat16, "o"), _ptr(o_ref, torch.bfloat16, "o_ref"), rows,
+        _ptr(sums, torch.float64, "sums"), _stream(stream)))
 
 
 def cb_hkvd_select_noalloc(v_new, v_old, cand, m, k, n_rows, sel_tok, sel_row, stream=None):

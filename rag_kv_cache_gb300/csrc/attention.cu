@@ -108,6 +108,14 @@ struct Params {
   float scale_log2;
   uint8_t* out;
   int32_t* err;
+  // Diagnostics (null in the blend): row_stats receives each row's (max, sum) of the softmax in
+  // log2 units, A_ij = 2^(s_ij * scale_log2 - max) / sum. The counting instance reads count_stats
+  // (such a pair per row) and writes to counts, per row, how many of the n_keys weights lie
+  // below 2^log2_eps (masked keys, weight 0, included).
+  float2* row_stats;
+  const float2* count_stats;
+  float log2_eps;
+  int32_t* counts;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -330,7 +338,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major)
          ((uint32_t)(m >> 4) << 24);
 }
 
-template <int D>
+template <int D, bool COUNT>
 __global__ void __launch_bounds__(kThreads, 1)
     hkvd_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -570,6 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // m_ref: reference max (log2 units) that this warpgroup's O and l are scaled to.
     float m_ref = -INFINITY, l = 0.0f;
     bool ok = true;
+    // counting instance: weights below eps are the scores below tau = max + log2(eps * sum)
+    float tau = 0.0f;
+    int cnt = 0;
+    if constexpr (COUNT) {
+      const int t = min(t0 + r / p.group, t_last);
+      const float2 st = p.count_stats[(size_t)t * p.hq + (size_t)g * p.group + (r % p.group)];
+      tau = st.x + p.log2_eps + __log2f(st.y);
+    }
     // Wait until P V_j is complete (barrier pv_done[j % 2], its phase j / 2). Polled: a
     // suspended waiter resumes late, and these waits sit on the tile loop's critical path.
     auto wait_pv = [&](int j, int site) -> bool {
@@ -597,6 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kHalf; ++c)
           if (c > lim) sv[c] = 0xff800000u;  // -inf
+      }
+      if constexpr (COUNT) {  // masked columns (-inf) count too; the epilogue corrects for the tile edge
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) cnt += __uint_as_float(sv[c]) * p.scale_log2 < tau ? 1 : 0;
       }
 
       // Row max of this half tile from the registers, before any exponential: the reference m_ref
@@ -678,8 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [warpgroup][max, sum][row] in the K ring: every K tile has been consumed by now (the last
     // P V is complete and the S MMAs before it), so the ring is free.
     float(*s_ml)[2][kBM] = reinterpret_cast<float(*)[2][kBM]>(smem_raw + (sK0 - smem_u32(smem_raw)));
+    int(*s_cnt)[kBM] = reinterpret_cast<int(*)[kBM]>(smem_raw + (sK0 - smem_u32(smem_raw)) + 4 * kBM * 4);
     s_ml[wg][0][r] = m_ref;
     s_ml[wg][1][r] = l;
+    if constexpr (COUNT) s_cnt[wg][r] = cnt;
     tc_fence_before();
     __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
@@ -690,10 +712,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mm = fmaxf(m0, m1);
       const float a0 = m0 == -INFINITY ? 0.0f : ex2(m0 - mm);
       const float a1 = m1 == -INFINITY ? 0.0f : ex2(m1 - mm);
-      const float inv = 1.0f / (s_ml[0][1][r] * a0 + s_ml[1][1][r] * a1);
+      const float sum = s_ml[0][1][r] * a0 + s_ml[1][1][r] * a1;
+      const float inv = 1.0f / sum;
       const int t = t0 + r / p.group;
       const bool valid = t <= t_last;
-      uint8_t* dst = p.out + ((size_t)t * p.hq + (size_t)g * p.group + (r % p.group)) * D * 2;
+      const size_t row = (size_t)t * p.hq + (size_t)g * p.group + (r % p.group);
+      uint8_t* dst = p.out + row * D * 2;
+      if (valid && p.row_stats != nullptr) p.row_stats[row] = make_float2(mm, sum);
+      // the visited tiles cover keys [0, 128 n_kv): keys past n_keys were counted as masked,
+      // keys past the last visited tile were not visited and are all masked for this row
+      if constexpr (COUNT)
+        if (valid) p.counts[row] = s_cnt[0][r] + s_cnt[1][r] + (p.n_keys - n_kv * kBN);
 #pragma unroll 1
       for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
         uint32_t o0[32], o1[32];
@@ -750,9 +779,10 @@ bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* 
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool COUNT>
 cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k, const void* v, int n_keys,
-                         int hq, int hkv, float scale, void* out, int32_t* err, cudaStream_t s) {
+                         int hq, int hkv, float scale, void* out, const AttentionDiag& diag, int32_t* err,
+                         cudaStream_t s) {
   const int group = hq / hkv;
   const int tq = kBM / group;
   const int n_qtiles = (mq + tq - 1) / tq;
@@ -781,26 +811,35 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = static_cast<uint8_t*>(out);
   p.err = err;
+  p.row_stats = diag.row_stats;
+  p.count_stats = diag.count_stats;
+  p.log2_eps = diag.log2_eps;
+  p.counts = diag.counts;
   size_t smem = 1024 + (size_t)(kBM + (kKStages + kVStages) * kBN) * D * 2;
   if (smem < 117 * 1024) smem = 117 * 1024;  // one CTA per SM: the CTA takes all 512 TMEM columns
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(hkvd_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(hkvd_attention_kernel<D, COUNT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(hkvd_attention_kernel<D>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map, p);
+  return launch_pdl(hkvd_attention_kernel<D, COUNT>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map, p);
 }
 
 }  // namespace
 
 cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, const void* k, const void* v,
                                   int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim, float scale, void* out,
-                                  int32_t* err, cudaStream_t s) {
+                                  int32_t* err, cudaStream_t s, const AttentionDiag& diag) {
   if (mq <= 0) return cudaSuccess;
-  if (head_dim == 128) return launch_typed<128>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
-  if (head_dim == 64) return launch_typed<64>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+  const bool count = diag.counts != nullptr;
+  if (head_dim == 128)
+    return count ? launch_typed<128, true>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s)
+                 : launch_typed<128, false>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s);
+  if (head_dim == 64)
+    return count ? launch_typed<64, true>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s)
+                 : launch_typed<64, false>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s);
   return cudaErrorInvalidValue;
 }
 

@@ -304,6 +304,56 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                      "cb_hkvd_attention");
 }
 
+cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
+                                const void* v, int32_t n_keys, float scale, float eps, void* out, void* row_stats,
+                                int32_t* counts, uint64_t* total, void* stream) {
+  CB_TRY(check_plan(plan));
+  if (mq < 0 || n_keys < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(CB_ERR_INVALID_ARG, "eps must be positive and finite");
+  CB_TRY(need_ptr(total, "total"));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mq == 0) return cuda_status(cudaMemsetAsync(total, 0, sizeof(uint64_t), s), "cb_attention_sparsity");
+  if (n_keys == 0) return fail(CB_ERR_INVALID_ARG, "n_keys == 0 with queries to answer");
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_ptr(q_pos, "q_pos"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  CB_TRY(need_tensor(out, "out"));
+  CB_TRY(need_tensor(row_stats, "row_stats"));
+  CB_TRY(need_ptr(counts, "counts"));
+  const auto& c = plan->cfg;
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)c.head_dim);
+  const cb::QueryPositions qp{q_pos, mq, 0, true};
+  cb::AttentionDiag first;  // pass 1: the attention and each row's (max, sum)
+  first.row_stats = static_cast<float2*>(row_stats);
+  CB_TRY(cuda_status(cb::launch_hkvd_attention(q, qp, mq, k, v, n_keys, c.hq, c.hkv, c.head_dim, scale, out, plan->err,
+                                               s, first),
+                     "cb_attention_sparsity (statistics pass)"));
+  cb::AttentionDiag second;  // pass 2: the same scores against each row's threshold
+  second.count_stats = static_cast<const float2*>(row_stats);
+  second.log2_eps = std::log2(eps);
+  second.counts = counts;
+  CB_TRY(cuda_status(cb::launch_hkvd_attention(q, qp, mq, k, v, n_keys, c.hq, c.hkv, c.head_dim, scale, out, plan->err,
+                                               s, second),
+                     "cb_attention_sparsity (counting pass)"));
+  return cuda_status(cb::launch_sum_counts(counts, (int64_t)mq * c.hq, reinterpret_cast<unsigned long long*>(total), s),
+                     "cb_attention_sparsity (sum)");
+}
+
+cb_status cb_output_deviation(cb_plan* plan, const void* o, const void* o_ref, int32_t rows, double* sums,
+                              void* stream) {
+  CB_TRY(check_plan(plan));
+  if (rows < 0) return fail(CB_ERR_INVALID_ARG, "rows < 0");
+  CB_TRY(need_ptr(sums, "sums"));
+  if (rows > 0) {
+    CB_TRY(need_tensor(o, "o"));
+    CB_TRY(need_tensor(o_ref, "o_ref"));
+  }
+  const int64_t n = (int64_t)rows * plan->cfg.hq * plan->cfg.head_dim;
+  return cuda_status(cb::launch_output_deviation(o, o_ref, n, sums, static_cast<cudaStream_t>(stream)),
+                     "cb_output_deviation");
+}
+
 cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
                               float scale, void* out, void* stream) {
   CB_TRY(check_plan(plan));

@@ -68,10 +68,28 @@ struct QueryPositions {
   bool wait_prior;
 };
 
+// Optional diagnostics of one attention launch (all null in the blend): row_stats receives each
+// (row, head)'s softmax (max, sum) in log2 units; with counts set, the launch also counts per
+// (row, head) the weights below 2^log2_eps over all n_keys keys, from count_stats (the row
+// statistics of an earlier launch on the same inputs).
+struct AttentionDiag {
+  float2* row_stats = nullptr;
+  const float2* count_stats = nullptr;
+  float log2_eps = 0.0f;
+  int32_t* counts = nullptr;
+};
+
 // Causal GQA attention over compact RoPE-encoded query rows.
 cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, const void* k,
                                   const void* v, int32_t n_keys, int32_t hq, int32_t hkv, int32_t head_dim,
-                                  float scale, void* out, int32_t* err, cudaStream_t s);
+                                  float scale, void* out, int32_t* err, cudaStream_t s,
+                                  const AttentionDiag& diag = AttentionDiag());
+
+// Diagnostics reductions. sum_counts: *total = sum of counts[0..n) (64-bit). output_deviation:
+// sums[0] = sum (a - b)^2, sums[1] = sum b^2 over n bf16 elements, in fp64 (order of the block
+// partials not fixed: the last bits may differ between runs).
+cudaError_t launch_sum_counts(const int32_t* counts, int64_t n, unsigned long long* total, cudaStream_t s);
+cudaError_t launch_output_deviation(const void* a, const void* b, int64_t n, double* sums, cudaStream_t s);
 
 // Scratch of the decode attention (owned by the plan): per (kv head, split, q head) an
 // unnormalised output row and its (max, sum), and one ticket counter per kv head that is
