@@ -29,6 +29,7 @@ Parity status per function:
   attention.decode_attention           pinned (last row of library causal attention, special cases)
   diagnostics.attention_deviation      pinned (definition, r = 100% gives exactly 0)
   diagnostics.attention_sparsity       pinned (closed form for equal scores, library softmax matrix)
+  projection.qkv_projection            pinned (element loops, one-hot rows, RoPE at the row position)
 """
 
-from . import attention, blend, deviation, diagnostics, fuse, positions, rope, topk  # noqa: F401
+from . import attention, blend, deviation, diagnostics, fuse, positions, projection, rope, topk  # noqa: F401

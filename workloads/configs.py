@@ -39,6 +39,8 @@ class BlendConfig:
     lognormal_mu: float = -4.0
     lognormal_sigma: float = 2.0
     sweep_pct: tuple = field(default_factory=tuple)
+    # hidden size of the model (the QKV projection's input width)
+    d_model: int = 0
 
     @property
     def n_ctx(self) -> int:
@@ -61,20 +63,20 @@ CONFIGS = {
     # 2 chunks x 256 + 32 suffix, 4 q / 2 kv heads, head_dim 64: small enough
     # for the CPU oracle to finish in seconds.
     "tiny": BlendConfig("tiny", 1, 2, 256, 32, 4, 2, 64, 1e4, 1, 15, 15,
-                        noise="set", hkvd_frac=0.15, swap_frac=0.0),
+                        noise="set", hkvd_frac=0.15, swap_frac=0.0, d_model=256),
     # Mistral-7B-shaped: 6 x 512 + 64, 32 q / 8 kv heads, head_dim 128, 32 layers.
     "mistral7b": BlendConfig("mistral7b", 2, 6, 512, 64, 32, 8, 128, 1e4, 32, 30, 15,
-                             noise="set", hkvd_frac=0.15, swap_frac=0.10),
+                             noise="set", hkvd_frac=0.15, swap_frac=0.10, d_model=4096),
     # Long-context Mistral-7B-shaped: 16 x 2048 + 128 (32,896 tokens), 32 layers.
     "long32k": BlendConfig("long32k", 3, 16, 2048, 128, 32, 8, 128, 1e4, 32, 30, 15,
-                           noise="set", hkvd_frac=0.15, swap_frac=0.10),
+                           noise="set", hkvd_frac=0.15, swap_frac=0.10, d_model=4096),
     # Llama-70B-shaped: 8 x 1024 + 256, 64 q / 8 kv heads, theta 5e5, 80 layers.
     "llama70b": BlendConfig("llama70b", 4, 8, 1024, 256, 64, 8, 128, 5e5, 80, 20, 10,
-                            noise="set", hkvd_frac=0.10, swap_frac=0.10),
+                            noise="set", hkvd_frac=0.10, swap_frac=0.10, d_model=8192),
     # Recompute-ratio sweep at Mistral shape, 16 x 512 + 64, one layer; the
     # lognormal per-token noise scale makes the top-k boundary dense with ties.
     "sweep": BlendConfig("sweep", 5, 16, 512, 64, 32, 8, 128, 1e4, 1, 15, 15,
-                         noise="lognormal", sweep_pct=(5, 10, 15, 30, 50, 100)),
+                         noise="lognormal", sweep_pct=(5, 10, 15, 30, 50, 100), d_model=4096),
 }
 
 

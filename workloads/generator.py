@@ -28,6 +28,7 @@ from .configs import BlendConfig
 _T_K_OLD, _T_V_OLD, _T_K_EPS, _T_V_EPS, _T_Q = 0, 1, 2, 3, 4
 _T_K_SUF, _T_V_SUF, _T_LOGN, _T_SETS = 5, 6, 7, 100
 _T_DEC_K, _T_DEC_V, _T_DEC_Q = 200, 201, 202
+_T_PROJ_X, _T_PROJ_W = 300, 301
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -137,3 +138,17 @@ def generate_decode(cfg: BlendConfig, layer: int, extra: int = 1) -> DecodeInput
     v = f32_to_bf16_bits(_rng(cfg, layer, _T_DEC_V).standard_normal((n, cfg.hkv, cfg.head_dim), dtype=np.float32))
     q = f32_to_bf16_bits(_rng(cfg, layer, _T_DEC_Q).standard_normal((cfg.hq, cfg.head_dim), dtype=np.float32))
     return DecodeInputs(layer, k, v, q)
+
+
+def generate_projection(cfg: BlendConfig, layer: int, d_model: int | None = None):
+    """The QKV projection's inputs for a layer: hidden rows x [n_tokens, d_model] ~ N(0, 1) and
+    a fused weight w [(hq + 2 hkv) * head_dim, d_model] ~ N(0, 1 / d_model) (random weights of
+    the model's shape; no trained weights), both as bf16 bits."""
+    dm = d_model or cfg.d_model
+    if dm <= 0:
+        raise ValueError("the workload has no hidden size")
+    n_out = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
+    x = f32_to_bf16_bits(_rng(cfg, layer, _T_PROJ_X).standard_normal((cfg.n_tokens, dm), dtype=np.float32))
+    w = f32_to_bf16_bits(_rng(cfg, layer, _T_PROJ_W).standard_normal((n_out, dm), dtype=np.float32)
+                         * np.float32(1.0 / np.sqrt(dm)))
+    return x, w
