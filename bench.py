@@ -59,10 +59,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--path", choices=["blend", "decode", "diagnostics"], default="blend",
+    ap.add_argument("--path", choices=["blend", "decode", "diagnostics", "projection"], default="blend",
                     help="blend: the per-layer blend (default); decode: one decode step's attention over "
                          "every layer's cache after the request; diagnostics: attention deviation of the "
-                         "fused cache from a full prefill over the recompute ratios, and attention sparsity")
+                         "fused cache from a full prefill over the recompute ratios, and attention sparsity; "
+                         "projection: the gathered QKV projection of every layer's recomputed rows")
     ap.add_argument("--eps", type=float, default=1e-3, help="sparsity threshold of the diagnostics path")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (smaller captures for profiling; not a bench line)")
@@ -639,6 +640,107 @@ def run_diagnostics(args, cfg):
     return 0
 
 
+def run_projection(args, cfg):
+    """Projection path: per step, the QKV projection (RoPE-encoded q and k) of every layer's
+    recomputed rows, at the blend's row counts (layer 1 all tokens, then C_l and the suffix).
+    Four distinct hidden-state / weight sets (random, of the model's shape) are cycled over the
+    layers, so a layer's weights are not in L2 from the layer before."""
+    import torch
+    import torch.distributed as dist
+
+    import rag_kv_cache_gb300 as cb
+    from rag_kv_cache_gb300.build import build
+    from workloads.generator import generate_projection
+    from workloads.torch_io import bf16_tensor
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    plan = cb.Plan.from_config(cfg)
+    sets = [generate_projection(cfg, s + 1) for s in range(min(4, cfg.layers))]
+    xs = [bf16_tensor(x, dev) for x, _ in sets]
+    ws = [bf16_tensor(w, dev) for _, w in sets]
+    rng = np.random.default_rng(cfg.config_id)
+    rows, sizes = [], []
+    for layer in range(1, cfg.layers + 1):
+        n_cand, k, mq, selects = plan.layer_sizes(layer)
+        if layer == 1:
+            r = np.arange(cfg.n_tokens)  # layer 1 recomputes every token
+        else:
+            r = np.concatenate([np.sort(rng.choice(cfg.n_ctx, n_cand, replace=False)),
+                                np.arange(cfg.n_ctx, cfg.n_tokens)])
+        rows.append(torch.as_tensor(r.astype(np.int32), device=dev))
+        sizes.append(r.size)
+    d_model = cfg.d_model
+    xg = torch.empty((cfg.n_tokens, d_model), dtype=torch.bfloat16, device=dev)
+    q = torch.empty((cfg.n_tokens, cfg.hq, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((cfg.n_tokens, cfg.hkv, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for li in range(cfg.layers):
+            s_ = li % len(sets)
+            cb.cb_qkv_projection(plan, xs[s_], rows[li], sizes[li], ws[s_], q, k, v, encode=True, x_gathered=xg,
+                                 stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    plan.check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clocks:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            stop.record(stream)
+        stream.synchronize()
+    ms = start.elapsed_time(stop) / args.steps
+    plan.check()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    n_out = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
+    flops = sum(2.0 * m_ * d_model * n_out for m_ in sizes)
+    peaks = load_peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "QKV projection TFLOP/s (recomputed rows of every layer)", "value": world * tf,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1) hidden rows, N(0, 1/d_model) weights of the model's shape",
+            "config": {"workload": workload_desc(cfg), "path": "projection", "d_model": d_model, "n_out": n_out,
+                       "rows_per_layer": sorted(set(sizes)), "cuda_graph": True,
+                       "l2": "four weight sets cycled (4 x %.0f MB)" % (n_out * d_model * 2 / 1e6)},
+            "roofline": {"kernel": "qkv_projection (with the row gather)", "bound": "tensor", "achieved": tf,
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 sustained", "flops_per_step": flops},
+            "gpu_launches": 2 * cfg.layers * args.steps, "clocks": clocks.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
     """Metric through the C ABI with host buffers: H2D of every layer's inputs and D2H of its outputs timed."""
     import torch
@@ -726,6 +828,8 @@ def main():
         return run_decode(args, cfg)
     if args.path == "diagnostics":
         return run_diagnostics(args, cfg)
+    if args.path == "projection":
+        return run_projection(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -190,6 +190,23 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                             const void* k, const void* v, int32_t n_keys, float scale, void* out,
                             void* stream);
 
+/* QKV projection of the rows a layer recomputes ("rag的kvcache问题" §阶段一: each token's q, k,
+ * v is its hidden vector times the projection weights, computed as one product of the stacked
+ * rows; §渐进式过滤机制: at a layer only the candidate tokens and the suffix are recomputed):
+ *   y_i = x[t] W^T,  t = rows ? rows[i] : i,  i in [0, m),
+ *   q[t] = y_i[Q heads], k[t] = y_i[K heads], v[t] = y_i[V heads]  (bf16),
+ * with q and k RoPE-encoded at position t (the plan's table and style) when `encode` != 0, and
+ * left before RoPE otherwise (the form cb_blend_layer reads as k_new / q). x: [x_rows, d_model]
+ * bf16 hidden rows, d_model a positive multiple of 64 (else CB_ERR_UNSUPPORTED). w_qkv:
+ * [(hq + 2 hkv) D, d_model] bf16, one output feature per row (Q heads, then K heads, then V
+ * heads). q: [n_tokens, hq, D], k, v: [n_tokens, hkv, D] of the plan, written only at the rows'
+ * tokens. With a row list, x_gathered (caller-owned, [m, d_model] bf16) receives the gathered rows
+ * first; NULL rows read x[0 .. m) in place. A row outside x (or past n_tokens) is recorded as
+ * CB_ERR_DEVICE_CHECK and not written. tcgen05 GEMM (bf16 in, fp32 accumulate) fed by TMA. */
+cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows,
+                            int32_t m, const void* w_qkv, int32_t encode, void* x_gathered, void* q, void* k, void* v,
+                            void* stream);
+
 /* Decode attention over a cache ("rag的kvcache问题" §阶段 2 (Decode): after the prefill the
  * newest token is the only query, and its [1, d] query row is matched against the whole
  * cached K/V, which makes the step memory-bound). For the newest token at position

@@ -108,4 +108,13 @@ cudaError_t launch_decode_attention(const void* q, const void* k, const void* v,
                                     int32_t hkv, int32_t head_dim, float scale, void* out, const DecodeScratch& ws,
                                     cudaStream_t s);
 
+// QKV projection of gathered rows (rows null: row i is token i, read from x directly; else the
+// rows are first copied to x_gathered [m, d_model]): q / k / v rows of token t = rows[i] from
+// x[t] W^T, q and k RoPE-encoded at position t when `encode`. W: [(hq + 2 hkv) head_dim, d_model].
+cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows, int32_t m,
+                                  void* x_gathered, const void* w, int32_t n_tokens, int32_t hq, int32_t hkv,
+                                  int32_t head_dim, int32_t encode, int32_t style, RopeTable t, void* q, void* k,
+                                  void* v, int32_t* err, cudaStream_t s);
+bool qkv_projection_supported(int32_t d_model);
+
 }  // namespace cb

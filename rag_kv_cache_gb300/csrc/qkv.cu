@@ -1,0 +1,357 @@
+// The step before the blend: the QKV projection of the rows a layer recomputes, on sm_103a
+// tensor cores ("rag的kvcache问题" §阶段一: each token's q, k, v is its hidden vector times the
+// projection weights, computed as one product of the stacked rows; §渐进式过滤机制: a layer
+// recomputes only its candidate tokens and the query suffix).
+//
+//   y[i, :] = x[rows[i], :] W^T,  W = W_qkv [(Hq + 2 Hkv) D, d_model] (one output feature per row)
+//   q[t] = y[i, Q heads], k[t] = y[i, K heads], v[t] = y[i, V heads],  t = rows[i],
+// with q and k optionally RoPE-encoded at position t (the plan's cos/sin table) in the epilogue,
+// all written token-indexed as bf16: the layout the blend reads its recomputed rows from.
+//
+// The candidate rows of X are first gathered into a contiguous workspace by a streaming kernel
+// (2 m d_model bytes each way): a 128-byte-swizzled TMA tile must land on a 1024-byte boundary,
+// which four-row gathers into one tile cannot all meet. One CTA per 128 x 256 output tile (128
+// gathered rows, two 128-wide heads or four 64-wide heads of one of Q, K, V). Warp 0 feeds a
+// 4-stage ring with TMA: the 128 x 64 slice of the gathered rows and the 256 x 64 slice of W,
+// both 128-byte swizzled; warp 1 issues tcgen05.mma (M 128, N 256, K 16; bf16 in,
+// fp32 accumulate in 256 TMEM columns), one commit per stage frees its slot; warps 4-7 (TMEM lanes
+// 0-127, one output row per thread) turn the finished accumulator into bf16 rows. Every mbarrier
+// wait is bounded (2 s); a timeout records an error, the CTA drains its copies and MMAs, frees
+// TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tmem_ops.cuh"
+
+namespace cb {
+namespace {
+
+constexpr int kPM = 128;  // gathered rows per tile
+constexpr int kPN = 256;  // output features per tile
+constexpr int kPK = 64;   // K slice per stage (one 128-byte swizzle row of bf16)
+constexpr int kPStages = 4;
+constexpr uint32_t kPABytes = kPM * kPK * 2;  // 16 KiB
+constexpr uint32_t kPBBytes = kPN * kPK * 2;  // 32 KiB
+constexpr int kPThreads = 256;
+constexpr uint32_t kPTmemCols = 256;
+
+struct ProjParams {
+  const int32_t* rows;  // token id of row i (null: row i is token i)
+  int m;
+  int n_tokens;
+  int d_model;
+  int hq, hkv, head_dim;
+  int encode;
+  int style;
+  const float2* tab;  // [n_tokens][head_dim / 2] (cos, sin)
+  uint8_t* q;
+  uint8_t* k;
+  uint8_t* v;
+  int32_t* err;
+};
+
+struct ProjBars {
+  uint64_t full[kPStages];
+  uint64_t empty[kPStages];
+  uint64_t acc_full;
+  uint64_t drain;
+};
+
+// Rows of X to a contiguous [m, d_model] buffer: one warp per row, 16-byte accesses; an index
+// outside X gives a zero row and an error record.
+__global__ void __launch_bounds__(256) gather_rows_kernel(uint8_t* dst, const uint8_t* src, const int32_t* rows,
+                                                          int m, int n_src, int row_bytes, int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (warp >= m) return;
+  const int t = rows[warp];
+  uint8_t* d = dst + (size_t)warp * row_bytes;
+  if (t < 0 || t >= n_src) {
+    if (lane == 0) record_error(err, kErrIndex, warp);
+    for (int c = lane * 16; c < row_bytes; c += 32 * 16) st_stream(d + c, make_uint4(0u, 0u, 0u, 0u));
+    return;
+  }
+  const uint8_t* sp = src + (size_t)t * row_bytes;
+  constexpr int B = 4;
+  for (int c0 = lane * 16; c0 < row_bytes; c0 += 32 * 16 * B) {
+    uint4 v[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+      if (c0 + b * 512 < row_bytes) v[b] = ld_stream(sp + c0 + b * 512);
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+      if (c0 + b * 512 < row_bytes) st_stream(d + c0 + b * 512, v[b]);
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 1)
+    qkv_projection_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                          const ProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ProjBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_rows[kPM];
+
+  pdl_launch_dependents();
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + kPStages * kPABytes;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int m0 = blockIdx.x * kPM;
+  const int n0 = blockIdx.y * kPN;
+  const int n_k = p.d_model / kPK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);
+      mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.acc_full), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kPTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_wait();  // the rows and hidden states come from the kernels before this one
+  // Token id of each of the tile's rows (-1: past m, or an index the gather rejected: not stored).
+  if (threadIdx.x < kPM) {
+    const int i = m0 + (int)threadIdx.x;
+    int t = i < p.m ? (p.rows ? p.rows[i] : i) : -1;
+    if (t >= p.n_tokens) t = -1;
+    s_rows[threadIdx.x] = t;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kk = 0; kk < n_k; ++kk) {
+        const int st = kk % kPStages;
+        if (kk >= kPStages &&
+            !mbar_wait(smem_u32(&bars.empty[st]), ((kk / kPStages) - 1) & 1, abort_flag, p.err, 40))
+          break;
+        const uint32_t fb = smem_u32(&bars.full[st]);
+        mbar_expect_tx(fb, kPABytes + kPBBytes);
+        tma_load_2d(sA0 + st * kPABytes, &tm_x, fb, kk * kPK, m0);  // rows past m read as zeros
+        tma_load_2d(sB0 + st * kPBBytes, &tm_w, fb, kk * kPK, n0);
+        issued = kk + 1;
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int kk = issued - kPStages < 0 ? 0 : issued - kPStages; kk < issued; ++kk)
+        mbar_wait(smem_u32(&bars.full[kk % kPStages]), (kk / kPStages) & 1, abort_flag, p.err, 41, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    constexpr uint32_t idesc = idesc_bf16(kPM, kPN, false);
+    const uint64_t da0 = sdesc(sA0, 16, 1024);
+    const uint64_t db0 = sdesc(sB0, 16, 1024);
+    bool ok = true;
+    for (int kk = 0; kk < n_k && ok; ++kk) {
+      const int st = kk % kPStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.full[st]), (kk / kPStages) & 1, abort_flag, p.err, 42));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t da = da0 + (uint64_t)((st * kPABytes) >> 4);
+        const uint64_t db = db0 + (uint64_t)((st * kPBBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kPK / 16; ++ks)
+          mma_ss(tmem, da + (uint64_t)((ks * 32) >> 4), db + (uint64_t)((ks * 32) >> 4), idesc,
+                 (kk > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&bars.empty[st]));
+        if (kk == n_k - 1) tc_commit(smem_u32(&bars.acc_full));
+      }
+      __syncwarp();
+    }
+    // all MMAs issued here complete before TMEM is freed
+    if (elect_one()) tc_commit(smem_u32(&bars.drain));
+    __syncwarp();
+    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 43, false);
+  } else if (warp >= 4) {
+    const int r = (warp - 4) * 32 + lane;  // TMEM lane = output row of the tile
+    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.acc_full), 0, abort_flag, p.err, 44));
+    if (ok) {
+      tc_fence_after();
+      const int t = s_rows[r];
+      const bool store = m0 + r < p.m && t >= 0;
+      constexpr int kHeads = kPN / D;
+#pragma unroll 1
+      for (int hh = 0; hh < kHeads; ++hh) {
+        const int f0 = n0 + hh * D;  // first output feature of this head
+        if (f0 >= (p.hq + 2 * p.hkv) * D) break;  // the last tile may reach past W (read as zeros)
+        uint8_t* dst;
+        bool rope;
+        if (f0 < p.hq * D) {
+          dst = p.q + ((size_t)t * p.hq + f0 / D) * D * 2;
+          rope = p.encode != 0;
+        } else if (f0 < (p.hq + p.hkv) * D) {
+          dst = p.k + ((size_t)t * p.hkv + (f0 / D - p.hq)) * D * 2;
+          rope = p.encode != 0;
+        } else {
+          dst = p.v + ((size_t)t * p.hkv + (f0 / D - p.hq - p.hkv)) * D * 2;
+          rope = false;
+        }
+        const uint32_t col = lane_base + hh * D;
+        if (rope && p.style == 0) {
+          // pairs (j, j + D/2): columns j0.. and D/2 + j0.. of the head
+          const float2* cs = p.tab + (size_t)(t < 0 ? 0 : t) * (D / 2);
+#pragma unroll 1
+          for (int j0 = 0; j0 < D / 2; j0 += 32) {
+            uint32_t a[32], b[32];
+            tmem_ld_x32(col + j0, a);
+            tmem_ld_x32(col + D / 2 + j0, b);
+            if (store) {
+              float oa[32], ob[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 c = cs[j0 + e];
+                const float x = __uint_as_float(a[e]), y = __uint_as_float(b[e]);
+                oa[e] = x * c.x - y * c.y;
+                ob[e] = x * c.y + y * c.x;
+              }
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                *reinterpret_cast<uint4*>(dst + (j0 + q4 * 8) * 2) = pack8(oa + q4 * 8);
+                *reinterpret_cast<uint4*>(dst + (D / 2 + j0 + q4 * 8) * 2) = pack8(ob + q4 * 8);
+              }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t a[32];
+            tmem_ld_x32(col + c0, a);
+            if (store) {
+              float o[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
+              if (rope) {  // pairs (2j, 2j + 1)
+                const float2* cs = p.tab + (size_t)t * (D / 2) + c0 / 2;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const float2 c = cs[e];
+                  const float x = o[2 * e], y = o[2 * e + 1];
+                  o[2 * e] = x * c.x - y * c.y;
+                  o[2 * e + 1] = x * c.y + y * c.x;
+                }
+              }
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) *reinterpret_cast<uint4*>(dst + (c0 + q4 * 8) * 2) = pack8(o + q4 * 8);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols) : "memory");
+  }
+}
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (enc == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_proj_typed(const ProjParams& p, const void* x, const void* w, cudaStream_t s) {
+  const int n_out = (p.hq + 2 * p.hkv) * D;
+  CUtensorMap tx, tw;
+  if (!encode_2d(&tx, x, (uint64_t)p.d_model, (uint64_t)p.m, kPK, kPM) ||
+      !encode_2d(&tw, w, (uint64_t)p.d_model, (uint64_t)n_out, kPK, kPN))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + (size_t)kPStages * (kPABytes + kPBBytes);
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(qkv_projection_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const dim3 grid((p.m + kPM - 1) / kPM, (n_out + kPN - 1) / kPN);
+  return launch_pdl(qkv_projection_kernel<D>, grid, kPThreads, smem, s, tx, tw, p);
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows, int32_t m,
+                                  void* x_gathered, const void* w, int32_t n_tokens, int32_t hq, int32_t hkv,
+                                  int32_t head_dim, int32_t encode, int32_t style, RopeTable t, void* q, void* k,
+                                  void* v, int32_t* err, cudaStream_t s) {
+  if (m <= 0) return cudaSuccess;
+  const void* a = x;
+  if (rows != nullptr) {  // gather the rows into the workspace first
+    const int blocks = (int)(((int64_t)m * 32 + 255) / 256);
+    const cudaError_t e = launch_pdl(gather_rows_kernel, blocks, 256, 0, s, (uint8_t*)x_gathered, (const uint8_t*)x,
+                                     rows, m, x_rows, d_model * 2, err);
+    if (e != cudaSuccess) return e;
+    a = x_gathered;
+  }
+  ProjParams p;
+  p.rows = rows;
+  p.m = m;
+  p.n_tokens = n_tokens;
+  p.d_model = d_model;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.head_dim = head_dim;
+  p.encode = encode;
+  p.style = style;
+  p.tab = t.tab;
+  p.q = static_cast<uint8_t*>(q);
+  p.k = static_cast<uint8_t*>(k);
+  p.v = static_cast<uint8_t*>(v);
+  p.err = err;
+  if (head_dim == 128) return launch_proj_typed<128>(p, a, w, s);
+  if (head_dim == 64) return launch_proj_typed<64>(p, a, w, s);
+  return cudaErrorInvalidValue;
+}
+
+bool qkv_projection_supported(int32_t d_model) { return d_model >= kPK && d_model % kPK == 0; }
+
+}  // namespace cb

@@ -1,0 +1,94 @@
+"""Gathered QKV projection (the step before the blend, "rag的kvcache问题" §阶段一) against the oracle.
+
+Written rows within 2e-2 abs + 1e-2 rel of the oracle's fp64 product rounded to bf16 (fp32
+accumulation, bf16 output); rows outside the list are left as they were, bit for bit.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_close_bf16
+from oracle.deviation import bf16_bits_to_f64
+from oracle.projection import qkv_projection
+from workloads import get_config
+from workloads.generator import generate_projection
+from workloads.torch_io import bf16_bits, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).cuda()
+
+
+def _run(cb, cfg, rows, m, encode, style="half", d_model=None):
+    plan = cb.Plan.from_config(cfg, rope_style=style)
+    x, w = generate_projection(cfg, 1, d_model)
+    n = cfg.n_tokens
+    sentinel = lambda h: torch.full((n, h, cfg.head_dim), 7.0, dtype=torch.bfloat16, device="cuda")
+    q, k, v = sentinel(cfg.hq), sentinel(cfg.hkv), sentinel(cfg.hkv)
+    xg = torch.empty((max(m, 1), x.shape[1]), dtype=torch.bfloat16, device="cuda") if rows is not None else None
+    cb.cb_qkv_projection(plan, bf16_tensor(x), None if rows is None else _i32(rows), m, bf16_tensor(w), q, k, v,
+                         encode=encode, x_gathered=xg)
+    plan.check()
+    plan.close()
+    tok = np.arange(m) if rows is None else np.asarray(rows)
+    oq, ok, ov = qkv_projection(bf16_bits_to_f64(x), tok, bf16_bits_to_f64(w), cfg.hq, cfg.hkv, cfg.head_dim,
+                                cfg.rope_theta, encode, style)
+    got = [bf16_bits_to_f64(bf16_bits(t)) for t in (q, k, v)]
+    for g, o, what in zip(got, (oq, ok, ov), "qkv"):
+        assert_close_bf16(g[tok], o, what=what)
+        untouched = np.setdiff1d(np.arange(n), tok)
+        assert np.all(g[untouched] == 7.0)
+    return got
+
+
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+@pytest.mark.parametrize("encode", [True, False])
+def test_tiny_gathered_rows(cb, style, encode):
+    cfg = get_config("tiny")
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([np.sort(rng.choice(cfg.n_ctx, 81, replace=False)), np.arange(cfg.n_ctx, cfg.n_tokens)])
+    _run(cb, cfg, rows, rows.size, encode, style)
+
+
+@pytest.mark.parametrize("m", [1, 127, 129, 300])
+def test_row_counts_and_in_place_rows(cb, m):
+    cfg = dataclasses.replace(get_config("tiny"), hq=8, hkv=1, head_dim=128, n_chunks=1, chunk_len=292, n_suffix=8)
+    _run(cb, cfg, None, m, True, d_model=64)  # one K slice; 1280 outputs = 5 tiles
+
+
+def test_partial_last_tile_of_w(cb):
+    cfg = dataclasses.replace(get_config("tiny"), hq=4, hkv=1, head_dim=64)  # 384 outputs: 1.5 tiles
+    rows = np.arange(0, cfg.n_tokens, 3)
+    _run(cb, cfg, rows, rows.size, True)
+
+
+@pytest.mark.parametrize("name,m", [("mistral7b", 985), ("llama70b", 300)])
+def test_model_shapes(cb, name, m):
+    cfg = get_config(name)
+    rng = np.random.default_rng(m)
+    n_suf = cfg.n_suffix
+    rows = np.concatenate([np.sort(rng.choice(cfg.n_ctx, m - n_suf, replace=False)),
+                           np.arange(cfg.n_ctx, cfg.n_tokens)])
+    _run(cb, cfg, rows, rows.size, True)
+
+
+def test_bad_row_is_recorded_and_skipped(cb):
+    cfg = get_config("tiny")
+    plan = cb.Plan.from_config(cfg)
+    x, w = generate_projection(cfg, 1)
+    q = torch.zeros((cfg.n_tokens, cfg.hq, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((cfg.n_tokens, cfg.hkv, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    xg = torch.empty((3, x.shape[1]), dtype=torch.bfloat16, device="cuda")
+    cb.cb_qkv_projection(plan, bf16_tensor(x), _i32([5, cfg.n_tokens + 3, 9]), 3, bf16_tensor(w), q, k, v, x_gathered=xg)
+    with pytest.raises(cb.CacheBlendError):
+        plan.check()
+    assert torch.count_nonzero(q[5]) > 0 and torch.count_nonzero(q[9]) > 0
+    with pytest.raises(cb.CacheBlendError):  # d_model not a multiple of 64
+        cb.cb_qkv_projection(plan, bf16_tensor(x[:, :100].copy()), None, 4, bf16_tensor(w[:, :100].copy()), q, k, v)
+    plan.close()
