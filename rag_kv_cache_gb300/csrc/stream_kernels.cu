@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __
 // Fused cache: 8 consecutive rows per block, one warp per row.
 constexpr int kFuseRows = 8;
 constexpr int kFuseThreads = 256;
+constexpr int kQParts = 4;  // warps per query row in the fused pass
 
 // First index j in the ascending list sel[0..k) with sel[j] >= key (k if none),
 // by one warp: 32-ary search, one coalesced probe and ballot per round.
@@ -501,9 +502,13 @@ __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
   const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
   const int kv_blocks = (n_tokens + kFuseRows - 1) / kFuseRows;
   if ((int)blockIdx.x >= kv_blocks) {
-    // query row i: token sel[i] (i < k) or n_ctx + i - k, encoded at its own position
-    const int i = ((int)blockIdx.x - kv_blocks) * kFuseRows + warp;
-    if (i >= mq) return;
+    // query row i: token sel[i] (i < k) or n_ctx + i - k, encoded at its own position; a row is
+    // shared by kQParts warps (each a contiguous group of heads), so every warp has one batch of
+    // loads in flight instead of several in turn
+    const int qw = ((int)blockIdx.x - kv_blocks) * kFuseRows + warp;
+    const int parts = (hq % kQParts == 0) ? kQParts : 1;
+    const int i = qw / kQParts, part = qw % kQParts;
+    if (i >= mq || part >= parts) return;
     const int tok = i < k ? sel[i] : n_ctx + (i - k);
     if (tok < 0 || tok >= n_tokens || (i < k && tok >= n_ctx)) {
       if (lane == 0) record_error(err, kErrIndex, i);
@@ -514,9 +519,25 @@ __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
       return;
     }
     const size_t q_bytes = (size_t)hq * head_dim * 2;
-    rotate_row<STYLE, 2>(q_rot + (size_t)i * q_bytes, q + (size_t)tok * q_bytes, hq, head_dim,
-                         t.tab + (size_t)tok * (head_dim / 2), false, lane);
+    const int part_heads = hq / parts;
+    const size_t part_off = (size_t)part * part_heads * head_dim * 2;
+    rotate_row<STYLE, 2>(q_rot + (size_t)i * q_bytes + part_off, q + (size_t)tok * q_bytes + part_off, part_heads,
+                         head_dim, t.tab + (size_t)tok * (head_dim / 2), false, lane);
     return;
+  }
+  // The row's source does not depend on the selection for suffix rows (always recomputed) and
+  // mostly is the cache for context rows: pull those lines into L2 while warp 0 reads the list.
+  {
+    const int tok = blockIdx.x * kFuseRows + warp;
+    if (tok < n_tokens) {
+      const size_t rb = (size_t)hkv * head_dim * 2;
+      const uint8_t* kp = (tok < n_ctx ? k_old : k_new) + tok * rb;
+      const uint8_t* vp = (tok < n_ctx ? v_old : v_new) + tok * rb;
+      for (size_t off = (size_t)lane * 128; off < rb; off += 32 * 128) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(kp + off));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(vp + off));
+      }
+    }
   }
   const int r0 = blockIdx.x * kFuseRows;
   if (out_tok != nullptr && threadIdx.x < kFuseRows) {
@@ -680,7 +701,7 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
                               const void* q, void* q_rot, int32_t mq, int32_t hq, int32_t* err, cudaStream_t s) {
   if (n_tokens <= 0) return cudaSuccess;
   if (q == nullptr || q_rot == nullptr) mq = 0;
-  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows + (mq + kFuseRows - 1) / kFuseRows;
+  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows + (mq * kQParts + kFuseRows - 1) / kFuseRows;
   auto* kf = (uint8_t*)k_fused;
   auto* vf = (uint8_t*)v_fused;
   if (style == 0)
