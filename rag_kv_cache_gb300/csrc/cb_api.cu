@@ -12,6 +12,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Streams that run consecutive layers' attention in cb_blend_request (the caller's stream and
+// CB_ATTN_STREAMS - 1 of the plan's): a layer's attention overlaps the tails of the layers before it.
+#ifndef CB_ATTN_STREAMS
+#define CB_ATTN_STREAMS 2
+#endif
+constexpr int kAttnStreams = CB_ATTN_STREAMS;
+static_assert(kAttnStreams >= 1 && kAttnStreams <= 8, "attention streams");
+
 struct cb_plan {
   cb_config cfg;
   int device;
@@ -20,7 +28,8 @@ struct cb_plan {
   float2* rope_tab;  // [n_tokens][head_dim / 2]
   int32_t* err;      // [0] flags, [1] first offending index (-1 = none)
   cudaStream_t aux_stream;  // cb_blend_request: every layer's deviation, top-k and fuse (with the query encoding)
-  cudaStream_t aux_attn;    // cb_blend_request: attention of even layers (odd layers on the caller's stream)
+  cudaStream_t aux_attn[kAttnStreams];  // cb_blend_request: attention of layer l on stream (l - 1) % kAttnStreams
+                                        // ([0] unused: that one is the caller's stream)
   cudaEvent_t ev_fork, ev_ready, ev_join;
   cb::DecodeScratch decode;  // cb_decode_attention's split partials and ticket counters
 };
@@ -120,7 +129,8 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
   if (e == cudaSuccess) e = cudaMalloc(&p->rope_tab, sizeof(float2) * (size_t)n_tokens * (c.head_dim / 2));
   if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux_stream, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux_attn, cudaStreamNonBlocking);
+  for (int a = 1; a < kAttnStreams && e == cudaSuccess; ++a)
+    e = cudaStreamCreateWithFlags(&p->aux_attn[a], cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
@@ -171,7 +181,8 @@ cb_status cb_plan_destroy(cb_plan* plan) {
   cudaFree(plan->decode.part_ml);
   cudaFree(plan->decode.tickets);
   if (plan->aux_stream) cudaStreamDestroy(plan->aux_stream);
-  if (plan->aux_attn) cudaStreamDestroy(plan->aux_attn);
+  for (int a = 1; a < kAttnStreams; ++a)
+    if (plan->aux_attn[a]) cudaStreamDestroy(plan->aux_attn[a]);
   if (plan->ev_fork) cudaEventDestroy(plan->ev_fork);
   if (plan->ev_ready) cudaEventDestroy(plan->ev_ready);
   if (plan->ev_join) cudaEventDestroy(plan->ev_join);
@@ -425,8 +436,10 @@ static cb_status validate_io(cb_plan* plan, int32_t layer, const cb_layer_io* io
 // One stage of layer `layer` on `s`; `cand` is the candidate list the layer reads (ignored at
 // layer 1, where the candidates are all context tokens). S_l is sel_tok at selecting layers and
 // the candidates themselves elsewhere; the fuse pass then copies them out to sel_tok / sel_row.
+// inputs_by_event: the attention's inputs are ordered by an event on its stream (cb_blend_request),
+// so it need not wait for the kernel before it on that stream, which it does not read from.
 static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, const int32_t* cand,
-                               const LayerShape& sh, int32_t stage, cudaStream_t s) {
+                               const LayerShape& sh, int32_t stage, cudaStream_t s, bool inputs_by_event = false) {
   const auto& c = plan->cfg;
   if (layer == 1) cand = nullptr;
   const int32_t* sel = sh.selects ? io->sel_tok : cand;
@@ -457,7 +470,7 @@ static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* 
     case CB_STAGE_ATTENTION: {
       if (sh.mq == 0) return CB_OK;
       // query row t sits at sel[t] (t < k) or n_ctx + t - k
-      const cb::QueryPositions qp{sel, sh.k, plan->n_ctx, true};
+      const cb::QueryPositions qp{sel, sh.k, plan->n_ctx, !inputs_by_event};
       return cuda_status(cb::launch_hkvd_attention(io->q_rot, qp, sh.mq, io->k_fused, io->v_fused, plan->n_tokens,
                                                    c.hq, c.hkv, c.head_dim, 1.0f / std::sqrt((float)c.head_dim),
                                                    io->out, plan->err, s),
@@ -500,10 +513,13 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
     CB_TRY(validate_io(plan, l, &ios[l - 1], cand_of(l), &sh));
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t attn_stream[2] = {s, plan->aux_attn};
+  cudaStream_t attn_stream[kAttnStreams];
+  attn_stream[0] = s;
+  for (int a = 1; a < kAttnStreams; ++a) attn_stream[a] = plan->aux_attn[a];
   CB_TRY(cuda_status(cudaEventRecord(plan->ev_fork, s), "fork"));
   CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_stream, plan->ev_fork, 0), "fork"));
-  CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_attn, plan->ev_fork, 0), "fork"));
+  for (int a = 1; a < kAttnStreams; ++a)
+    CB_TRY(cuda_status(cudaStreamWaitEvent(attn_stream[a], plan->ev_fork, 0), "fork"));
   for (int32_t l = 1; l <= n_layers; ++l) {
     const cb_layer_io* io = &ios[l - 1];
     const int32_t* cand = cand_of(l);
@@ -511,13 +527,15 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
     CB_TRY(validate_io(plan, l, io, cand, &sh));
     for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_FUSE; ++st)
       CB_TRY(enqueue_stage(plan, l, io, cand, sh, st, plan->aux_stream));
-    const cudaStream_t a = attn_stream[(l - 1) & 1];
+    const cudaStream_t a = attn_stream[(l - 1) % kAttnStreams];
     CB_TRY(cuda_status(cudaEventRecord(plan->ev_ready, plan->aux_stream), "layer inputs ready"));
     CB_TRY(cuda_status(cudaStreamWaitEvent(a, plan->ev_ready, 0), "layer inputs ready"));
-    CB_TRY(enqueue_stage(plan, l, io, cand, sh, CB_STAGE_ATTENTION, a));
+    CB_TRY(enqueue_stage(plan, l, io, cand, sh, CB_STAGE_ATTENTION, a, true));
   }
-  CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, plan->aux_attn), "join"));
-  CB_TRY(cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join"));
+  for (int a = 1; a < kAttnStreams; ++a) {
+    CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, attn_stream[a]), "join"));
+    CB_TRY(cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join"));
+  }
   CB_TRY(cuda_status(cudaEventRecord(plan->ev_join, plan->aux_stream), "join"));
   return cuda_status(cudaStreamWaitEvent(s, plan->ev_join, 0), "join");
 }
