@@ -81,6 +81,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, device, world):
+    """The largest value of x over the ranks (the slowest rank's time); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units all ranks processed per second, over the slowest rank's time in ms."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def workload_desc(cfg):
     return (f"{cfg.name}: {cfg.n_chunks}x{cfg.chunk_len} cached + {cfg.n_suffix} suffix tokens, "
             f"{cfg.hq} q / {cfg.hkv} kv heads, head_dim {cfg.head_dim}, RoPE theta {cfg.rope_theta:g}, "
@@ -362,12 +379,9 @@ def run_ours(args, cfg):
     with ClockSampler(gpu_index) as clocks:
         elapsed_ms = timed(run_steps)
     plan.check()
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     ms_per_step = elapsed_ms / args.steps
-    value = cfg.n_ctx * cfg.layers * args.steps * world / (elapsed_ms / 1e3)
+    value = whole_job_rate(cfg.n_ctx * cfg.layers * args.steps, world, elapsed_ms)
 
     # Per-kernel times: one graph per stage holding that stage's kernel for every layer that has
     # it (cb_blend_stage; each stage rewrites its outputs from its inputs, so replays are idempotent).
@@ -500,10 +514,7 @@ def run_decode(args, cfg):
         stream.synchronize()
     ms = start.elapsed_time(stop)
     plan.check()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
     ms_step = ms / args.steps
     row_kv = cfg.hkv * cfg.head_dim * 2
     bytes_launch = 2.0 * n_keys * row_kv + 2.0 * cfg.hq * cfg.head_dim * 2
@@ -713,10 +724,7 @@ def run_projection(args, cfg):
         stream.synchronize()
     ms = start.elapsed_time(stop) / args.steps
     plan.check()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
     n_out = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
     flops = sum(2.0 * m_ * d_model * n_out for m_ in sizes)
     peaks = load_peaks()
@@ -798,11 +806,8 @@ def run_e2e(args, cfg, cb, plan, host_inputs, bufs, sizes, dev, world):
     comp.wait_stream(h2d)
     stop.record(comp)
     torch.cuda.synchronize(dev)
-    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(start.elapsed_time(stop), dev, world)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     plan.check()
     return {"value": cfg.n_ctx * cfg.layers * args.e2e_steps * world / (ms / 1e3), "unit": UNIT,
