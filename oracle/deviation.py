@@ -65,7 +65,7 @@ def _bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 def deviation_fp64(v_new: np.ndarray, v_old: np.ndarray) -> np.ndarray:
     """sum over heads and dims of (v_new - v_old)^2 per token, in fp64 (plain order)."""
     d = np.asarray(v_new, dtype=np.float64) - np.asarray(v_old, dtype=np.float64)
-    return (d * d).reshape(d.shape[0], -1).sum(axis=1)
+    return (d * d).reshape(d.shape[0], int(np.prod(d.shape[1:]))).sum(axis=1)
 
 
 def key_deviation_fp64(k_new, k_old, p_old, p_new, theta: float, style: str = "half") -> np.ndarray:
@@ -77,7 +77,7 @@ def key_deviation_fp64(k_new, k_old, p_old, p_new, theta: float, style: str = "h
     a = rope_rotate(k_new, p_new, theta, style)
     b = rerotate(k_old, p_old, p_new, theta, style)
     d = a - b
-    return (d * d).reshape(d.shape[0], -1).sum(axis=1)
+    return (d * d).reshape(d.shape[0], int(np.prod(d.shape[1:]))).sum(axis=1)
 
 
 def kv_deviation_fp64(k_new, k_old, v_new, v_old, p_old, p_new, theta: float, style: str = "half") -> np.ndarray:
@@ -111,9 +111,9 @@ def _canonical_sum(parts) -> np.ndarray:
 
 def deviation_canonical_f32(v_new_bits: np.ndarray, v_old_bits: np.ndarray) -> np.ndarray:
     """fp32 deviation per token in the canonical order; inputs are bf16 bits [m, Hkv, D]."""
-    m = v_new_bits.shape[0]
-    vn = _bf16_bits_to_f32(v_new_bits).reshape(m, -1)
-    vo = _bf16_bits_to_f32(v_old_bits).reshape(m, -1)
+    m, e = v_new_bits.shape[0], int(np.prod(v_new_bits.shape[1:]))
+    vn = _bf16_bits_to_f32(v_new_bits).reshape(m, e)
+    vo = _bf16_bits_to_f32(v_old_bits).reshape(m, e)
     return _canonical_sum([vn - vo])
 
 
@@ -136,6 +136,7 @@ def kv_deviation_canonical_f32(k_new_bits, k_old_bits, v_new_bits, v_old_bits, p
     cos_t, sin_t = rope_table_f32(p_old, d, theta)
     kn = _bf16_bits_to_f32(k_new_bits).reshape(m, hkv, d)
     ko = _bf16_bits_to_f32(k_old_bits).reshape(m, hkv, d)
-    dk = (rotate_f32(kn, cos_t, sin_t, style) - ko).reshape(m, -1)
-    dv = _bf16_bits_to_f32(v_new_bits).reshape(m, -1) - _bf16_bits_to_f32(v_old_bits).reshape(m, -1)
+    e = hkv * d
+    dk = (rotate_f32(kn, cos_t, sin_t, style) - ko).reshape(m, e)
+    dv = _bf16_bits_to_f32(v_new_bits).reshape(m, e) - _bf16_bits_to_f32(v_old_bits).reshape(m, e)
     return _canonical_sum([dk, dv])

@@ -242,3 +242,12 @@ def test_rotate_f32_identity_turn_is_bitwise():
     x = np.array([[[1.5, -2.0, -0.0, 3.0]]], np.float32)
     out = rotate_f32(x, np.ones((1, 2), np.float32), np.zeros((1, 2), np.float32), "interleaved")
     np.testing.assert_array_equal(out.view(np.uint32), x.view(np.uint32))
+
+
+def test_empty_candidate_set_has_no_deviations():
+    # a layer whose candidate set is empty (r = 0 selects nothing at layer 1) ranks nothing
+    empty = np.zeros((0, 8, 128), np.uint16)
+    assert deviation_canonical_f32(empty, empty).shape == (0,)
+    assert deviation_fp64(empty.astype(np.float64), empty.astype(np.float64)).shape == (0,)
+    got = kv_deviation_canonical_f32(empty, empty, empty, empty, np.zeros(0, np.int64), 1e4)
+    assert got.shape == (0,)
