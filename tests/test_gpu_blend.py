@@ -208,3 +208,23 @@ def test_stages_one_by_one_match_the_layer_call(cb):
     with pytest.raises(cb.CacheBlendError):
         cb.cb_blend_stage(plan, 1, "fuse", cand=None, bufs=staged[0], **dict(ins[0], q=None))
     plan.close()
+
+
+@pytest.mark.parametrize("case", ["no_hkvd", "no_suffix", "ragged", "single_chunk"])
+def test_degenerate_requests(cb, case):
+    # r = 0 (only the suffix attends), no suffix (only the HKVD rows attend), chunk lengths and
+    # suffixes that fill no tile, and a single chunk (nothing is re-rotated)
+    base = get_config("mistral7b")
+    kw = dict(no_hkvd=dict(n_chunks=3, chunk_len=100, n_suffix=20, r1_pct=0, r2_pct=0),
+              no_suffix=dict(n_chunks=3, chunk_len=100, n_suffix=0),
+              ragged=dict(n_chunks=3, chunk_len=77, n_suffix=5, hq=8, hkv=2, head_dim=64),
+              single_chunk=dict(n_chunks=1, chunk_len=300, n_suffix=12))[case]
+    cfg = dataclasses.replace(base, name=case, config_id=95, layers=3, **kw)
+    g = run_gpu_layers(cb, cfg, [1, 2, 3])
+    o = oracle_layers(cfg, [1, 2, 3])
+    for layer in (1, 2, 3):
+        compare(g[layer], o[layer], cfg)
+        if case == "no_hkvd":
+            assert g[layer]["k"] == 0 and g[layer]["mq"] == cfg.n_suffix
+        if case == "no_suffix":
+            assert g[layer]["mq"] == g[layer]["k"]
