@@ -152,7 +152,8 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 template <int D, bool COUNT>
 __global__ void __launch_bounds__(kThreads, 1)
     hkvd_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                          const Params p) {
   constexpr int kBoxes = D / 64;
   constexpr uint32_t kQBytes = kBM * D * 2;
   constexpr uint32_t kKVBytes = kBN * D * 2;
@@ -509,6 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [warpgroup][max, sum][row] in the K ring: every K tile has been consumed by now (the last
     // P V is complete and the S MMAs before it), so the ring is free.
     float(*s_ml)[2][kBM] = reinterpret_cast<float(*)[2][kBM]>(smem_raw + (sK0 - smem_u32(smem_raw)));
+    // the output's staging boxes in the V ring, also free now (the last P V has completed)
+    constexpr uint32_t kOutBox = kBM * 128;
+    const uint32_t sOut = sV0;
     int(*s_cnt)[kBM] = reinterpret_cast<int(*)[kBM]>(smem_raw + (sK0 - smem_u32(smem_raw)) + 4 * kBM * 4);
     s_ml[wg][0][r] = m_ref;
     s_ml[wg][1][r] = l;
@@ -528,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = t0 + r / p.group;
       const bool valid = t <= t_last;
       const size_t row = (size_t)t * p.hq + (size_t)g * p.group + (r % p.group);
-      uint8_t* dst = p.out + row * D * 2;
       if (valid && p.row_stats != nullptr) p.row_stats[row] = make_float2(mm, sum);
       // the visited tiles cover keys [0, 128 n_kv): keys past n_keys were counted as masked,
       // keys past the last visited tile were not visited and are all masked for this row
@@ -541,20 +544,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_x32_async(lane_base + col_o(1, D) + c0, o1);
         tmem_wait_ld(o0);
         tmem_wait_ld(o1);
-        if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float f[8];
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float v0 = __uint_as_float(o0[q * 8 + e]) * a0;
-              const float v1 = __uint_as_float(o1[q * 8 + e]) * a1;
-              f[e] = (v0 + v1) * inv;
-            }
-            *reinterpret_cast<uint4*>(dst + (c0 + q * 8) * 2) = pack8(f);
+          for (int e = 0; e < 8; ++e) {
+            const float v0 = __uint_as_float(o0[q * 8 + e]) * a0;
+            const float v1 = __uint_as_float(o1[q * 8 + e]) * a1;
+            f[e] = (v0 + v1) * inv;
           }
+          // row r of the output box holding columns c: 128-byte rows, 16-byte chunks swizzled
+          const int c = c0 + q * 8;
+          const uint32_t dst = sOut + (uint32_t)(c / 64) * kOutBox + (uint32_t)r * 128u +
+                               (uint32_t)((((c % 64) / 8) ^ (r & 7)) * 16);
+          const uint4 pk = pack8(f);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y), "r"(pk.z),
+                       "r"(pk.w)
+                       : "memory");
         }
       }
+    }
+    // The tile's rows are one box of the output (TQ tokens x G heads x 64 columns, as Q was loaded):
+    // one TMA store per 64 columns; rows past mq are clipped by the tensor map.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
+    if (threadIdx.x == 0 && !*abort_flag) {
+#pragma unroll
+      for (int b = 0; b < kBoxes; ++b)
+        asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                         &tm_o),
+                     "r"(b * 64), "r"(0), "r"(g), "r"(t0), "r"(sOut + b * kOutBox)
+                     : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the box has left shared memory
     }
   }
 
@@ -597,7 +620,7 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   const int group = hq / hkv;
   const int tq = kBM / group;
   const int n_qtiles = (mq + tq - 1) / tq;
-  CUtensorMap tq_map, tk_map, tv_map;
+  CUtensorMap tq_map, tk_map, tv_map, to_map;
   const cuuint64_t qd[4] = {(cuuint64_t)D, (cuuint64_t)group, (cuuint64_t)hkv, (cuuint64_t)mq};
   const cuuint64_t qs[3] = {(cuuint64_t)D * 2, (cuuint64_t)group * D * 2, (cuuint64_t)hq * D * 2};
   const cuuint32_t qb[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)tq};
@@ -605,7 +628,7 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   const cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2};
   const cuuint32_t kbx[3] = {64, 1, (cuuint32_t)kBN};  // a K or V tile: kBN keys of one kv head
   if (!encode_map(&tq_map, q, 4, qd, qs, qb) || !encode_map(&tk_map, k, 3, kd, ks, kbx) ||
-      !encode_map(&tv_map, v, 3, kd, ks, kbx))
+      !encode_map(&tv_map, v, 3, kd, ks, kbx) || !encode_map(&to_map, out, 4, qd, qs, qb))
     return cudaErrorInvalidValue;
   Params p;
   p.pos_idx = qp.idx;
@@ -635,7 +658,8 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_pdl(hkvd_attention_kernel<D, COUNT>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map, p);
+  return launch_pdl(hkvd_attention_kernel<D, COUNT>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map,
+                    to_map, p);
 }
 
 }  // namespace
