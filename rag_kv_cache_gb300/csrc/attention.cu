@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // waiter -> issuer: the TMA inputs of the first round / of round j (slot j % 2) are in shared
   // memory (0: a wait gave up). Two slots: the waiter's write for round j + 1 cannot overtake the
   // issuer's read for round j, which precedes its arrival for round j + 1.
-  __shared__ int s_first_ok;
+  __shared__ int s_first_ok;   // Q and K_0 are in (S_0 may be issued)
+  __shared__ int s_second_ok;  // K_1 is in too (S_1 may be issued)
   __shared__ int s_round_ok[2];
 
   pdl_launch_dependents();
@@ -294,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = nv - kVStages < 0 ? 0 : nv - kVStages; j < nv; ++j)
         mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
     } else if (warp == kWarpMma || warp == kWarpWaiter) {
-      // Rounds: round -1 issues S_0 and S_1; round j issues P V_j and then S_{j+2} into the same
+      // Rounds: round -1 issues S_0 (once Q and K_0 are in) and then S_1 (once K_1 is, after a
+      // second meeting of issuer and waiter); round j issues P V_j and then S_{j+2} into the same
       // buffer. The waiter polls the TMA barriers a round needs (Q and K_0, K_1; then V_j and
       // K_{j+2}) and publishes whether they completed; the issuer and the waiter then meet the
       // softmax warps, whose joining says P_j is in TMEM, on named barrier kBarRound (round -1:
@@ -307,12 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto k_ready = [&](int j) {
           return spin_all(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, 11);
         };
-        bool ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0) && (n_kv < 2 || k_ready(1));
+        // S_0 goes out as soon as Q and K_0 are in, S_1 once K_1 is (it was requested after the
+        // query positions were known).
+        bool ok = spin_all(smem_u32(&bars.q_full), 0, 10) && k_ready(0);
         if (lane == 0) s_first_ok = ok ? 1 : 0;
         // bar.sync is warp-aligned: the warp must reach it converged, not split by the lane-0
         // store above (a split warp's arrivals can be counted in the wrong phase).
         __syncwarp();
         asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
+        if (n_kv > 1) {
+          ok = ok && k_ready(1);
+          if (lane == 0) s_second_ok = ok ? 1 : 0;
+          __syncwarp();
+          asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
+        }
         for (int j = 0; j < n_kv; ++j) {
           // every round is joined, also after a failure (the issuer then skips its MMAs)
           ok = ok && spin_all(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, 13) &&
@@ -345,11 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = s_first_ok != 0;
         if (ok) {
           tc_fence_after();
-          if (elect_one()) {
-            issue_s(0);
-            if (n_kv > 1) issue_s(1);
-          }
+          if (elect_one()) issue_s(0);
           __syncwarp();
+        }
+        if (n_kv > 1) {
+          __syncwarp();
+          asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
+          ok = ok && s_second_ok != 0;
+          if (ok) {
+            tc_fence_after();
+            if (elect_one()) issue_s(1);
+            __syncwarp();
+          }
         }
         for (int j = 0; j < n_kv; ++j) {
           __syncwarp();
