@@ -352,3 +352,32 @@ def test_attention_first_tile_scores_far_below_zero(cb):
     got = bf16_bits_to_f64(bf16_bits(out))
     assert np.all(np.isfinite(got))
     assert_close_bf16(got, ref, what="attention with very negative first-tile scores")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 2, 64)])
+def test_attention_tiles_mixing_early_and_late_rows(cb, hq, hkv, d):
+    # Query tiles that mix rows at the start of the cache with rows near its end: the early rows
+    # see only the first key tile and are masked in every later one, while the late rows attend
+    # to the whole cache. A second call on the same plan must give the same bits.
+    n_keys = 3100
+    tq = 128 // (hq // hkv)
+    q_pos = np.concatenate([np.arange(0, tq // 2), np.arange(n_keys - tq // 2 - 40, n_keys - 40),
+                            np.arange(1000, 1000 + tq), np.arange(n_keys - tq, n_keys)])
+    q_pos = np.unique(q_pos)
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=n_keys - 1, n_suffix=1)
+    plan = _plan(cb, cfg)
+    rng = np.random.default_rng(hq + hkv)
+    mq = q_pos.size
+    q = f32_to_bf16_bits((2.0 * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    outs = []
+    for _ in range(2):
+        out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+        plan.check()
+        outs.append(bf16_bits(out))
+    assert np.array_equal(outs[0], outs[1])
+    ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    assert_close_bf16(bf16_bits_to_f64(outs[0]), ref, what="attention with early and late rows in one tile")
