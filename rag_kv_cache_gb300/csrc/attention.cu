@@ -80,14 +80,19 @@ __host__ __device__ constexpr uint32_t col_s(int b, int h) { return (uint32_t)(b
 __host__ __device__ constexpr uint32_t col_o(int h, int d) { return 256u + (uint32_t)(h * d); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
+// One MMA commit per product: S_j's completion frees K stage j % 3 and tells the softmax that S_j
+// is in TMEM (both wait on s_done[j % 3], phase j / 3); P V_j's completion frees V stage j % 3 and
+// tells the softmax that O holds tile j (pv_done[j % 3]). A commit costs the tensor pipe ~30
+// cycles, so sharing one barrier between the two waiters of each product saves two per round.
+// The phases cannot alias: S_{j+3} is issued only after the softmax has finished tile j + 1, and
+// P V_{j+3} only after it has finished tile j + 3.
+static_assert(kKStages == 3 && kVStages == 3, "the S and P V barriers are indexed by the K and V stages");
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];
+  uint64_t s_done[kKStages];  // S_j complete: K stage j % 3 free and S_j readable (MMA commit)
   uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
-  uint64_t s_full[2];   // S_j in TMEM buffer j % 2 (MMA commit); phase j / 2
-  uint64_t pv_done[2];  // P_j V_j accumulated into both O (MMA commit); phase j / 2
+  uint64_t pv_done[kVStages];  // P V_j complete: V stage j % 3 free and O updated (MMA commit)
   uint64_t drain;
 };
 
@@ -189,15 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars.q_full), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
-      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+      mbar_init(smem_u32(&bars.s_done[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&bars.v_full[s]), 1);
-      mbar_init(smem_u32(&bars.v_empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bars.s_full[b]), 1);
-      mbar_init(smem_u32(&bars.pv_done[b]), 1);
+      mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
     mbar_init(smem_u32(&bars.drain), 1);
     s_abort = 0;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 1; j < n_kv; ++j) {
         const int sk = j % kKStages;
         if (j >= kKStages &&
-            !mbar_wait(smem_u32(&bars.k_empty[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1))
+            !mbar_wait(smem_u32(&bars.s_done[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1))
           break;
         const uint32_t kb = smem_u32(&bars.k_full[sk]);
         mbar_expect_tx(kb, kKVBytes);
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 1; j < n_kv; ++j) {
         const int sv = j % kVStages;
         if (j >= kVStages &&
-            !mbar_wait(smem_u32(&bars.v_empty[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2))
+            !mbar_wait(smem_u32(&bars.pv_done[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2))
           break;
         const uint32_t vb = smem_u32(&bars.v_full[sv]);
         mbar_expect_tx(vb, kKVBytes);
@@ -347,8 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + col_s(b, 0), dq + (uint64_t)((bx * kQBox + kk * 32) >> 4),
                    dk + (uint64_t)((bx * kKVBox + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&bars.k_empty[st]));
-          tc_commit(smem_u32(&bars.s_full[b]));
+          tc_commit(smem_u32(&bars.s_done[st]));
         };
         __syncwarp();
         asm volatile("bar.sync %0, 64;" ::"n"(kBarIssue) : "memory");
@@ -387,8 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ts(tmem + col_o(h, D), tmem + col_s(b, h) + ks * 8,
                        dv + (uint64_t)(((h * (kHalf / 16) + ks) * 16 * 128) >> 4), idesc_o, ks > 0 ? 1u : acc0);
             }
-            tc_commit(smem_u32(&bars.v_empty[st]));
-            tc_commit(smem_u32(&bars.pv_done[b]));
+            tc_commit(smem_u32(&bars.pv_done[st]));
             if (j + 2 < n_kv) issue_s(j + 2);
           }
           __syncwarp();
@@ -415,16 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 st = p.count_stats[(size_t)t * p.hq + (size_t)g * p.group + (r % p.group)];
       tau = st.x + p.log2_eps + __log2f(st.y);
     }
-    // Wait until P V_j is complete (barrier pv_done[j % 2], its phase j / 2). Polled: a
+    // Wait until P V_j is complete (barrier pv_done[j % 3], its phase j / 3). Polled: a
     // suspended waiter resumes late, and these waits sit on the tile loop's critical path.
     auto wait_pv = [&](int j, int site) -> bool {
-      const bool w = mbar_spin(smem_u32(&bars.pv_done[j & 1]), (j >> 1) & 1, abort_flag, p.err, site);
+      const bool w = mbar_spin(smem_u32(&bars.pv_done[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, site);
       return __all_sync(0xffffffffu, w);
     };
     // One tile; false if a wait gave up (the abort flag is raised then).
     auto tile = [&](int j) -> bool {
       const int b = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.s_full[b]), (j >> 1) & 1, abort_flag, p.err, 20 + wg)))
+      if (!__all_sync(0xffffffffu,
+                      mbar_spin(smem_u32(&bars.s_done[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 20 + wg)))
         return false;
       tc_fence_after();
       // Copy this half's 64 scores to registers; P_j is later written over their first 32 columns.
