@@ -190,7 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = tile * p.tq;
   const int t_last = min(t0 + p.tq, p.mq) - 1;
 
-  if (threadIdx.x == 0) {
+  // The producer thread initialises the barriers and starts the loads of Q and of the first K and
+  // V tiles at once: they do not depend on the query positions (every query tile sees key tile 0),
+  // so they overlap warp 0's TMEM allocation and the softmax threads' reads of the positions.
+  if (warp == kWarpProducer && lane == 0) {
     mbar_init(smem_u32(&bars.q_full), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 1);
@@ -205,20 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_maxpos = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  __syncthreads();
-  // The query rows, positions and fused K/V come from the kernels before this one on the stream.
-  if (p.wait_prior) pdl_wait();
-
-  // Q and the first K and V tiles do not depend on the query positions (every query tile sees
-  // key tile 0): their loads start before the positions are read.
-  if (warp == kWarpProducer && lane == 0) {
+    // The query rows and fused K/V come from the kernels before this one on the stream.
+    if (p.wait_prior) pdl_wait();
     const uint32_t qb = smem_u32(&bars.q_full);
     mbar_expect_tx(qb, kQBytes);
 #pragma unroll
@@ -227,12 +218,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_expect_tx(kb, kKVBytes);
 #pragma unroll
     for (int b = 0; b < kBoxes; ++b) tma_load_3d(sK0 + b * kKVBox, &tm_k, kb, b * 64, g, 0);
-  } else if (warp == kWarpProducerV && lane == 0) {
     const uint32_t vb = smem_u32(&bars.v_full[0]);
     mbar_expect_tx(vb, kKVBytes);
 #pragma unroll
     for (int b = 0; b < kBoxes; ++b) tma_load_3d(sV0 + b * kKVBox, &tm_v, vb, b * 64, g, 0);
   }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  // The positions come from the kernels before this one on the stream.
+  if (p.wait_prior) pdl_wait();
 
   // Query position of each softmax thread's row; padded rows repeat the tile's last token.
   int my_pos = 0;
