@@ -17,8 +17,9 @@
 //              own running max / sum and its own O accumulator, so the two
 //              halves of a tile are exponentiated at the same time; the two
 //              partial results are merged in the epilogue.
-//   warp 8     TMA producer of Q (once) and of K tiles (3-stage ring; a stage
-//              is refilled as soon as its S = Q K^T is done);
+//   warp 8     initialises the barriers and requests Q, K_0 and V_0 at entry, then
+//              is the TMA producer of the K tiles (3-stage ring; a stage is
+//              refilled as soon as its S = Q K^T is done);
 //   warp 9     issuer of both products (tcgen05.mma, bf16 in, fp32 accumulate);
 //   warp 10    TMA producer of V tiles (3-stage ring, refilled after P V);
 //   warp 11    the issuer's waiter: it polls the TMA barriers a round of MMAs
