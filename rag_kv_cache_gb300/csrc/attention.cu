@@ -554,27 +554,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // keys past the last visited tile were not visited and are all masked for this row
       if constexpr (COUNT)
         if (valid) p.counts[row] = s_cnt[0][r] + s_cnt[1][r] + (p.n_keys - n_kv * kBN);
-#pragma unroll 1
-      for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
-        uint32_t o0[32], o1[32];
-        tmem_ld_x32_async(lane_base + col_o(0, D) + c0, o0);
-        tmem_ld_x32_async(lane_base + col_o(1, D) + c0, o1);
-        tmem_wait_ld(o0);
-        tmem_wait_ld(o1);
+      // out = O_0 (a_0 / sum) + O_1 (a_1 / sum): both chunks' loads issued before one wait
+      const float b0 = a0 * inv, b1 = a1 * inv;
+      constexpr int kChunks = (D / 2) / 32;
+      uint32_t o0[kChunks][32], o1[kChunks][32];
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        tmem_ld_x32_async(lane_base + col_o(0, D) + wg * (D / 2) + ch * 32, o0[ch]);
+        tmem_ld_x32_async(lane_base + col_o(1, D) + wg * (D / 2) + ch * 32, o1[ch]);
+      }
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        tmem_wait_ld(o0[ch]);
+        tmem_wait_ld(o1[ch]);
+      }
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float v0 = __uint_as_float(o0[q * 8 + e]) * a0;
-            const float v1 = __uint_as_float(o1[q * 8 + e]) * a1;
-            f[e] = (v0 + v1) * inv;
-          }
+          for (int e = 0; e < 8; ++e)
+            f[e] = fmaf(__uint_as_float(o0[ch][q * 8 + e]), b0, __uint_as_float(o1[ch][q * 8 + e]) * b1);
+          const int c = wg * (D / 2) + ch * 32 + q * 8;
+          const uint4 pk = pack8(f);
           // row r of the output box holding columns c: 128-byte rows, 16-byte chunks swizzled
-          const int c = c0 + q * 8;
           const uint32_t dst = sOut + (uint32_t)(c / 64) * kOutBox + (uint32_t)r * 128u +
                                (uint32_t)((((c % 64) / 8) ^ (r & 7)) * 16);
-          const uint4 pk = pack8(f);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y), "r"(pk.z),
                        "r"(pk.w)
                        : "memory");
