@@ -674,13 +674,9 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   p.counts = diag.counts;
   size_t smem = 1024 + (size_t)(kBM + (kKStages + kVStages) * kBN) * D * 2;
   if (smem < 117 * 1024) smem = 117 * 1024;  // one CTA per SM: the CTA takes all 512 TMEM columns
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(hkvd_attention_kernel<D, COUNT>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t e = set_smem_limit_once(hkvd_attention_kernel<D, COUNT>, (int)smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(hkvd_attention_kernel<D, COUNT>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map,
                     to_map, p);
 }

@@ -306,13 +306,9 @@ cudaError_t launch_proj_typed(const ProjParams& p, const void* x, const void* w,
       !encode_2d(&tw, w, (uint64_t)p.d_model, (uint64_t)n_out, kPK, kPN))
     return cudaErrorInvalidValue;
   const size_t smem = 1024 + (size_t)kPStages * (kPABytes + kPBBytes);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(qkv_projection_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t e = set_smem_limit_once(qkv_projection_kernel<D>, (int)smem, configured);
+  if (e != cudaSuccess) return e;
   const dim3 grid((p.m + kPM - 1) / kPM, (n_out + kPN - 1) / kPN);
   return launch_pdl(qkv_projection_kernel<D>, grid, kPThreads, smem, s, tx, tw, p);
 }
