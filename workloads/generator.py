@@ -32,11 +32,26 @@ _T_PROJ_X, _T_PROJ_W = 300, 301
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bits."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    lsb = (b >> np.uint32(16)) & np.uint32(1)
-    r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
-    return r.astype(np.uint16)
+    """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Per element: (b + 0x7FFF + ((b >> 16) & 1)) >> 16 on the fp32 bit pattern b, modulo 2^32. Done
+    in blocks of 2^20 elements with one scratch buffer, so large tensors do not allocate several
+    full-size temporaries."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    b = a.view(np.uint32).reshape(-1)
+    out = np.empty(b.shape, dtype=np.uint16)
+    block = 1 << 20
+    t = np.empty(min(block, b.size), dtype=np.uint32)
+    for i in range(0, b.size, block):
+        src = b[i:i + block]
+        w = t[:src.size]
+        np.right_shift(src, np.uint32(16), out=w)
+        np.bitwise_and(w, np.uint32(1), out=w)
+        np.add(w, np.uint32(0x7FFF), out=w)
+        np.add(w, src, out=w)
+        np.right_shift(w, np.uint32(16), out=w)
+        out[i:i + block] = w
+    return out.reshape(a.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
