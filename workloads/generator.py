@@ -124,11 +124,16 @@ def generate_layer(cfg: BlendConfig, layer: int, sets: list | None = None) -> La
 
     k_new = np.empty((n, hkv, d), dtype=np.uint16)
     v_new = np.empty((n, hkv, d), dtype=np.uint16)
+    # recomputed = cached + s * eps, in fp32 (in place on eps), rounded once to bf16
     k_eps = _rng(cfg, layer, _T_K_EPS).standard_normal((n_ctx, hkv, d), dtype=np.float32)
-    k_new[:n_ctx] = f32_to_bf16_bits(bf16_bits_to_f32(k_old) + s * k_eps)
+    np.multiply(k_eps, s, out=k_eps)
+    np.add(k_eps, bf16_bits_to_f32(k_old), out=k_eps)
+    k_new[:n_ctx] = f32_to_bf16_bits(k_eps)
     del k_eps
     v_eps = _rng(cfg, layer, _T_V_EPS).standard_normal((n_ctx, hkv, d), dtype=np.float32)
-    v_new[:n_ctx] = f32_to_bf16_bits(bf16_bits_to_f32(v_old) + s * v_eps)
+    np.multiply(v_eps, s, out=v_eps)
+    np.add(v_eps, bf16_bits_to_f32(v_old), out=v_eps)
+    v_new[:n_ctx] = f32_to_bf16_bits(v_eps)
     del v_eps
     n_suf = cfg.n_suffix
     k_new[n_ctx:] = f32_to_bf16_bits(_rng(cfg, layer, _T_K_SUF).standard_normal((n_suf, hkv, d), dtype=np.float32))
