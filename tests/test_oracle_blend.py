@@ -2,6 +2,7 @@
 and the gradual filter's structure, on the seeded workloads."""
 
 import dataclasses
+import os
 
 import numpy as np
 import torch
@@ -146,3 +147,33 @@ def test_kv_deviation_mode_ranks_by_the_kv_number():
     np.testing.assert_array_equal(res.dev.view(np.uint32), dev.view(np.uint32))
     kth = np.sort(dev)[::-1][k - 1]
     assert np.all(dev[res.sel_tok] >= kth) and np.sum(dev > kth) <= k
+
+
+def test_gradual_filter_golden_example():
+    # tests/golden/gradual_filter.txt: three layers worked by hand from the page's description
+    from oracle.topk import hkvd_topk
+
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "gradual_filter.txt")
+    lines = [ln for ln in open(path, encoding="utf-8").read().splitlines() if ln and not ln.startswith("#")]
+    n_ctx = int(lines[0].split("|")[1])
+    r1, r2 = (int(x) for x in lines[1].split("|")[1].split())
+    layers = []
+    for ln in lines[2:]:
+        f = [x.strip() for x in ln.split("|")]
+        layers.append((int(f[0]), np.array(f[1].split(), dtype=np.int64),
+                       None if f[2] == "-" else np.array(f[2].split(), dtype=np.float64),
+                       np.array(f[3].split(), dtype=np.int64)))
+    schedule = gradual_filter_schedule(n_ctx, len(layers), r1, r2)
+    selections = {0: np.arange(n_ctx)}
+    for (layer, cand_want, dev, sel_want), (l2, k, selects) in zip(layers, schedule):
+        assert layer == l2
+        cand = selections[candidate_layer(layer)]
+        assert np.array_equal(cand, cand_want)
+        if selects:
+            sel, rows = hkvd_topk(dev, cand, k)
+            assert np.array_equal(cand[rows], sel)
+        else:
+            assert dev is None and k == cand.size
+            sel = cand
+        assert np.array_equal(sel, sel_want)
+        selections[layer] = sel
