@@ -23,9 +23,8 @@ Parity status per function:
   topk.hkvd_topk                       pinned (brute-force rank counting, ties, k = 0 / m)
   fuse.fused_kv                        pinned (definition, provenance)
   attention.causal_gqa_attention       pinned (library causal attention, single key, equal scores)
-  blend.gradual_filter_schedule        pinned in the default reading (a three-layer example worked
-                                       by hand from the page's illustration, structure); the
-                                       re-selection reading: parity unpinned beyond structure
+  blend.gradual_filter_schedule        pinned (three-layer examples worked by hand from the page's
+                                       illustration, one per reading; structure)
   deviation.kv_deviation_canonical_f32 pinned (closed form, frame invariance, plain loops, bound)
   attention.decode_attention           pinned (last row of library causal attention, special cases)
   diagnostics.attention_deviation      pinned (definition, r = 100% gives exactly 0)

@@ -5,6 +5,7 @@ import dataclasses
 import os
 
 import numpy as np
+import pytest
 import torch
 
 from oracle.blend import blend_layer, blend_request, candidate_layer, gradual_filter_schedule
@@ -149,11 +150,13 @@ def test_kv_deviation_mode_ranks_by_the_kv_number():
     assert np.all(dev[res.sel_tok] >= kth) and np.sum(dev > kth) <= k
 
 
-def test_gradual_filter_golden_example():
-    # tests/golden/gradual_filter.txt: three layers worked by hand from the page's description
+@pytest.mark.parametrize("fixture,filter", [("gradual_filter.txt", "keep"), ("gradual_filter_reselect.txt", "reselect")])
+def test_gradual_filter_golden_example(fixture, filter):
+    # tests/golden/gradual_filter*.txt: three layers worked by hand from the page's description,
+    # in the default reading and in the re-selection reading
     from oracle.topk import hkvd_topk
 
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "gradual_filter.txt")
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", fixture)
     lines = [ln for ln in open(path, encoding="utf-8").read().splitlines() if ln and not ln.startswith("#")]
     n_ctx = int(lines[0].split("|")[1])
     r1, r2 = (int(x) for x in lines[1].split("|")[1].split())
@@ -163,11 +166,11 @@ def test_gradual_filter_golden_example():
         layers.append((int(f[0]), np.array(f[1].split(), dtype=np.int64),
                        None if f[2] == "-" else np.array(f[2].split(), dtype=np.float64),
                        np.array(f[3].split(), dtype=np.int64)))
-    schedule = gradual_filter_schedule(n_ctx, len(layers), r1, r2)
+    schedule = gradual_filter_schedule(n_ctx, len(layers), r1, r2, filter)
     selections = {0: np.arange(n_ctx)}
     for (layer, cand_want, dev, sel_want), (l2, k, selects) in zip(layers, schedule):
         assert layer == l2
-        cand = selections[candidate_layer(layer)]
+        cand = selections[candidate_layer(layer, filter)]
         assert np.array_equal(cand, cand_want)
         if selects:
             sel, rows = hkvd_topk(dev, cand, k)
