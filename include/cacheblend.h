@@ -317,8 +317,11 @@ cb_status cb_blend_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, in
  * CB_NOALLOC_MAX_CANDIDATES floats (256 KiB) on every GPU that loads it,
  * held until the process exits; m above that limit returns
  * CB_ERR_INVALID_ARG. The first call on a device looks up that array's device
- * address (once per device, with the device current), so make the first call
- * on each device before any stream capture. All calls share the array: calls
+ * address (with the device current) and remembers it with the ID of the
+ * CUDA context it belongs to; a call that finds another context current on
+ * the device (after cudaDeviceReset, say) looks it up again. Make the first
+ * call on each device, and the first after such a reset, before any stream
+ * capture. All calls share the array: calls
  * whose work overlaps on the GPU (different streams, no ordering between
  * them) race and can return wrong selections; order them on one stream.
  * Device-side argument findings are not recorded (there is no plan to hold an

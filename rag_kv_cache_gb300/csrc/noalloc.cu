@@ -9,6 +9,8 @@
 // kernels as cb_kv_deviation + cb_hkvd_topk, but keeps the per-candidate
 // deviations (the only intermediate) in a fixed array compiled into the
 // library instead of a buffer someone has to allocate.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "../../include/cacheblend.h"
@@ -25,28 +27,69 @@ namespace {
 // held by every GPU that loads the library until the process exits.
 static __device__ __align__(256) float g_select_scratch[CB_NOALLOC_MAX_CANDIDATES];
 
+// The array's device address, per device, together with the ID of the CUDA context it was
+// looked up in. A context that is torn down and created again (cudaDeviceReset, or a primary
+// context released by its last user) reloads the library's module, and the array may then sit
+// at another address: a call that finds a different context ID on its device looks it up again.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  float* ptr;
+};
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-float* g_scratch_ptr[kMaxDevices] = {};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
 cb_status noalloc_fail(cb_status s, const char* msg) { return cb::set_last_error(s, msg); }
 
-// Device address of the scratch array on the current device. The array's name
-// in host code is only a host-side stand-in, so the address is asked for once
-// per device with that device current and remembered.
+template <typename Fn>
+bool driver_entry(const char* name, int version, Fn* out) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || p == nullptr)
+    return false;
+  *out = reinterpret_cast<Fn>(p);
+  return true;
+}
+
+// ID of the context current on this thread; 0 if none is current yet.
+cudaError_t current_context_id(unsigned long long* id) {
+  *id = 0;
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) return cudaSuccess;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array in the current device's current context. The array's name
+// in host code is only a host-side stand-in, so the address is asked for with the device current
+// (once per device and context) and remembered.
 cudaError_t scratch_on_current_device(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_ctx_current == nullptr &&
+      !(driver_entry("cuCtxGetCurrent", 4000, &g_ctx_current) && driver_entry("cuCtxGetId", 12000, &g_ctx_id)))
+    return cudaErrorNotSupported;
+  unsigned long long id = 0;
+  e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  if (id == 0 || g_scratch[dev].ptr == nullptr || g_scratch[dev].ctx_id != id) {
+    // The lookup also makes the device's primary context current if none was yet.
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_select_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    g_scratch[dev] = ScratchAddr{id, static_cast<float*>(p)};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 
