@@ -50,6 +50,8 @@ sys.path.insert(0, ROOT)
 METRIC = "context tokens blended/s per layer"
 UNIT = "tokens/s"
 STAGES = ("deviation", "topk", "fuse", "attention")
+DEFAULT_WORKLOAD = {"blend": "long32k", "sweep": "sweep", "decode": "long32k", "diagnostics": "sweep",
+                    "projection": "mistral7b"}
 
 
 def parse_args():
@@ -58,13 +60,17 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="long32k")
+    ap.add_argument("--workload", default=None,
+                    help="workload name (default: long32k for the blend and decode paths, sweep for the sweep "
+                         "and diagnostics paths, mistral7b for the projection path)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--path", choices=["blend", "decode", "diagnostics", "projection"], default="blend",
-                    help="blend: the per-layer blend (default); decode: one decode step's attention over "
+    ap.add_argument("--path", choices=["blend", "sweep", "decode", "diagnostics", "projection"], default="blend",
+                    help="blend: the per-layer blend (default); sweep: the single-layer blend at every "
+                         "recompute ratio of the ratio-sweep workload, L2 flushed between repetitions; "
+                         "decode: one decode step's attention over "
                          "every layer's cache after the request; diagnostics: attention deviation of the "
                          "fused cache from a full prefill over the recompute ratios, and attention sparsity; "
                          "projection: the gathered QKV projection of every layer's recomputed rows")
@@ -409,14 +415,15 @@ def stage_applies(name, size):
     return {"deviation": bool(selects), "topk": bool(selects), "fuse": True, "attention": mq > 0}[name]
 
 
-def traffic_for(kernel_src):
-    """dram bytes per launch from the committed ncu summary, if it was taken on this source."""
+def traffic_for(kernel_src, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel source on this
+    workload, if it was taken on the current source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         src = open(os.path.join(ROOT, "rag_kv_cache_gb300", "csrc", kernel_src), "rb").read()
-        entry = rec.get(kernel_src)
+        entry = rec.get(f"{kernel_src}@{workload}")
         if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
             return entry
     except (OSError, ValueError):
@@ -570,7 +577,7 @@ def run_ours(args, cfg):
     attn_s = stage_ms["attention"] / 1e3
     achieved_tf = float(flops.sum()) / attn_s / 1e12
     peak_tf = peaks["bf16_tflops_sustained"]
-    traffic = traffic_for("attention.cu")
+    traffic = traffic_for("attention.cu", cfg.name)
     roofline = {"kernel": "hkvd_attention", "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
@@ -614,6 +621,129 @@ def run_ours(args, cfg):
     plan.close()
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args, cfg):
+    """Sweep path: the single-layer blend at every recompute ratio r of the workload (r1 = r2 = r),
+    each repetition timed alone with the L2 flushed before it (a 512 MB write), median over
+    `steps` repetitions. Per r: the whole layer (cb_blend_layer) and each stage alone
+    (cb_blend_stage). At r = 100% every context row is recomputed, so the blend must equal a full
+    prefill's attention: the encoded cache, and the attention of every row over it by the same
+    kernels outside the blend, are compared bit for bit."""
+    import dataclasses
+
+    import torch
+
+    import rag_kv_cache_gb300 as cb
+    from rag_kv_cache_gb300.build import build
+    from workloads.generator import generate_layer
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    build()
+    dev = torch.device("cuda", local)
+    ratios = list(cfg.sweep_pct) or [cfg.r1_pct]
+    inp = generate_layer(cfg, 1)
+    d_in = {name: t.to(dev) for name, t in pinned_layer(inp).pinned.items()}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    peaks = load_peaks()
+    rows, check, launches = [], None, 0
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]
+
+    def timed_median(fn_graph):
+        ts = []
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                flush.fill_(1)
+                a.record(stream)
+                fn_graph.replay()
+                b.record(stream)
+        stream.synchronize()
+        ts = [a.elapsed_time(b) for a, b in ev]
+        return statistics.median(ts)
+
+    with ClockSampler(gpu_index) as clocks:
+        for r in ratios:
+            rcfg = dataclasses.replace(cfg, r1_pct=r, r2_pct=r, layers=1)
+            plan = cb.Plan.from_config(rcfg)
+            bufs = cb.LayerBuffers(plan, dev)
+            n_cand, k, mq, selects = plan.layer_sizes(1)
+
+            def layer(plan=plan, bufs=bufs):
+                cb.cb_blend_layer(plan, 1, cand=None, bufs=bufs, stream=stream, **d_in)
+
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    layer()
+            stream.synchronize()
+            plan.check()
+            graphs = {}
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer()
+            graphs["layer"] = g
+            for name in STAGES:
+                if not stage_applies(name, (n_cand, k, mq, selects)):
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    cb.cb_blend_stage(plan, 1, name, cand=None, bufs=bufs, stream=stream, **d_in)
+                graphs[name] = g
+            ms = {name: timed_median(g) for name, g in graphs.items()}
+            launches += args.steps * 2 * (len(graphs) - 1)  # the layer graph holds one launch per stage
+            plan.check()
+            flops = attention_flops(rcfg, bufs.sel_tok[:k].cpu().numpy())
+            b = stage_bytes(rcfg, n_cand, k, mq, selects)
+            row = {"r_pct": r, "k": k, "mq": mq, "ms_layer": ms["layer"],
+                   "tokens_per_s": cfg.n_ctx / (ms["layer"] / 1e3),
+                   "attention_flops": flops, "attention_us": 1e3 * ms["attention"],
+                   "attention_tflops": flops / (ms["attention"] / 1e3) / 1e12,
+                   "attention_frac": flops / (ms["attention"] / 1e3) / 1e12 / peaks["bf16_tflops"],
+                   "fuse_us": 1e3 * ms["fuse"],
+                   "fuse_frac_hbm": b["fuse"] / (ms["fuse"] / 1e3) / 1e9 / peaks["hbm_gbs"]}
+            if "deviation" in ms:
+                row.update({"deviation_us": 1e3 * ms["deviation"],
+                            "deviation_frac_hbm": b["deviation"] / (ms["deviation"] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                            "topk_us": 1e3 * ms["topk"]})
+            rows.append(row)
+            if r == 100:
+                # full prefill by the same kernels outside the blend: every key and query encoded at
+                # its position, then causal attention of all rows over the recomputed cache
+                n = cfg.n_tokens
+                pos = torch.arange(n, dtype=torch.int32, device=dev)
+                k_full = torch.empty_like(d_in["k_new"])
+                q_all = torch.empty((n, cfg.hq, cfg.head_dim), dtype=torch.bfloat16, device=dev)
+                o_full = torch.empty_like(q_all)
+                with torch.cuda.stream(stream):
+                    layer()
+                    cb.cb_rope_rerotate(plan, k_full, d_in["k_new"], pos, stream=stream)
+                    cb.cb_rope_rerotate(plan, q_all, d_in["q"], pos, stream=stream)
+                    cb.cb_hkvd_attention(plan, q_all, pos, n, k_full, d_in["v_new"], n, o_full, stream=stream)
+                stream.synchronize()
+                plan.check()
+                same = lambda a, b_: bool(torch.equal(a.view(torch.int16), b_.view(torch.int16)))
+                check = {"fused_k_equals_encoded_k_new": same(bufs.k_fused, k_full),
+                         "fused_v_equals_v_new": same(bufs.v_fused, d_in["v_new"]),
+                         "out_equals_full_prefill": same(bufs.out[:mq], o_full),
+                         "max_abs_diff": float((bufs.out[:mq].float() - o_full.float()).abs().max())}
+            plan.close()
+    base = next((x for x in rows if x["r_pct"] == cfg.r1_pct), rows[0])
+    line = {"metric": METRIC, "value": base["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": base["ms_layer"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": data_desc(cfg),
+            "config": {"workload": workload_desc(cfg), "path": "sweep", "n_ctx": cfg.n_ctx,
+                       "value_at_r_pct": base["r_pct"], "cuda_graph": True,
+                       "l2": "flushed before every repetition (512 MB write, outside the timed region)",
+                       "attention_peak": "measured bf16 burst (one launch timed alone)"},
+            "sweep": rows, "r100_full_recompute_check": check,
+            "gpu_launches": launches, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -981,6 +1111,8 @@ def main():
         args.warmup = 3
     from workloads import get_config
 
+    if args.workload is None:
+        args.workload = DEFAULT_WORKLOAD[args.path]
     cfg = get_config(args.workload)
     if args.layers is not None:
         import dataclasses
@@ -988,6 +1120,8 @@ def main():
         cfg = dataclasses.replace(cfg, layers=max(1, min(cfg.layers, args.layers)))
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.path == "sweep":
+        return run_sweep(args, cfg)
     if args.path == "decode":
         return run_decode(args, cfg)
     if args.path == "diagnostics":
