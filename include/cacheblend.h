@@ -332,6 +332,19 @@ cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int
                                  int32_t k, int32_t n_rows, int32_t hkv, int32_t head_dim,
                                  int32_t* sel_tok, int32_t* sel_row, void* stream);
 
+/* Test support for the failure path, not part of the blend (the pages have
+ * no counterpart). Runs cb_hkvd_attention's kernel (head_dim 128 only) in a
+ * form whose K-tile producer never requests key tile 1 and whose bounded
+ * waits give up after 100 us instead of 2 s: every CTA whose queries reach
+ * that tile (a query position >= 128) records CB_ERR_TIMEOUT in the plan's
+ * error word, skips its remaining rounds, waits (again bounded) for its own
+ * copies and tensor-core work, frees its tensor memory and returns, leaving
+ * its rows of `out` unwritten. The next cb_check reports CB_ERR_TIMEOUT and
+ * clears the word, and the device stays usable. Arguments as
+ * cb_hkvd_attention; CB_ERR_INVALID_ARG if n_keys <= 128 or mq <= 0. */
+cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq,
+                                         const void* k, const void* v, int32_t n_keys, void* out, void* stream);
+
 /* Synchronise the plan's device, read and clear its error word. Returns
  * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
  * cb_last_error_string). Off the hot path. */

@@ -155,7 +155,10 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return r;
 }
 
-template <int D, bool COUNT>
+// PROBE: the wait-timeout probe (test support only): the K producer never requests key tile 1
+// and every wait gives up after kProbeTimeoutNs, so the CTA takes its failure path (timeout
+// recorded, remaining rounds skipped, copies and tensor-core work drained, TMEM freed).
+template <int D, bool COUNT, bool PROBE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     hkvd_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kKVBytes = kBN * D * 2;
   constexpr uint32_t kQBox = kBM * 128;   // bytes of one 64-column box of Q
   constexpr uint32_t kKVBox = kBN * 128;  // bytes of one 64-column box of a K or V tile
+  constexpr uint64_t kLimit = PROBE ? kProbeTimeoutNs : kTimeoutNs;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
@@ -266,8 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 1; j < n_kv; ++j) {
         const int sk = j % kKStages;
         if (j >= kKStages &&
-            !mbar_wait(smem_u32(&bars.s_done[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1))
+            !mbar_wait(smem_u32(&bars.s_done[sk]), ((j / kKStages) - 1) & 1, abort_flag, p.err, 1, true, kLimit))
           break;
+        if constexpr (PROBE) {
+          if (j == 1) {  // never requested: every wait on this tile runs into its limit
+            nk = j + 1;
+            continue;
+          }
+        }
         const uint32_t kb = smem_u32(&bars.k_full[sk]);
         mbar_expect_tx(kb, kKVBytes);
 #pragma unroll
@@ -276,15 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         nk = j + 1;
       }
       // Before the CTA can exit, every copy issued must have landed.
-      mbar_wait(qb, 0, abort_flag, p.err, 3, false);
+      mbar_wait(qb, 0, abort_flag, p.err, 3, false, kLimit);
       for (int j = nk - kKStages < 0 ? 0 : nk - kKStages; j < nk; ++j)
-        mbar_wait(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 4, false);
+        mbar_wait(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 4, false, kLimit);
     } else if (warp == kWarpProducerV && lane == 0) {
       int nv = 1;  // V tile 0 is in flight already
       for (int j = 1; j < n_kv; ++j) {
         const int sv = j % kVStages;
         if (j >= kVStages &&
-            !mbar_wait(smem_u32(&bars.pv_done[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2))
+            !mbar_wait(smem_u32(&bars.pv_done[sv]), ((j / kVStages) - 1) & 1, abort_flag, p.err, 2, true, kLimit))
           break;
         const uint32_t vb = smem_u32(&bars.v_full[sv]);
         mbar_expect_tx(vb, kKVBytes);
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nv = j + 1;
       }
       for (int j = nv - kVStages < 0 ? 0 : nv - kVStages; j < nv; ++j)
-        mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false);
+        mbar_wait(smem_u32(&bars.v_full[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, 5, false, kLimit);
     } else if (warp == kWarpMma || warp == kWarpWaiter) {
       // Rounds: round -1 issues S_0 (once Q and K_0 are in) and then S_1 (once K_1 is, after a
       // second meeting of issuer and waiter); round j issues P V_j and then S_{j+2} into the same
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arrival; an mbarrier polled by a busy warp was noticed hundreds of cycles late.
       if (warp == kWarpWaiter) {
         auto spin_all = [&](uint32_t bar, uint32_t parity, int site) -> bool {
-          return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site));
+          return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site, kLimit));
         };
         auto k_ready = [&](int j) {
           return spin_all(smem_u32(&bars.k_full[j % kKStages]), (j / kKStages) & 1, 11);
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // All tensor-core work issued by this CTA completes before TMEM is freed.
         if (elect_one()) tc_commit(smem_u32(&bars.drain));
         __syncwarp();
-        mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 14, false);
+        mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 14, false, kLimit);
       }
     }
     __syncwarp();
@@ -417,14 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Wait until P V_j is complete (barrier pv_done[j % 3], its phase j / 3). Polled: a
     // suspended waiter resumes late, and these waits sit on the tile loop's critical path.
     auto wait_pv = [&](int j, int site) -> bool {
-      const bool w = mbar_spin(smem_u32(&bars.pv_done[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, site);
+      const bool w =
+          mbar_spin(smem_u32(&bars.pv_done[j % kVStages]), (j / kVStages) & 1, abort_flag, p.err, site, kLimit);
       return __all_sync(0xffffffffu, w);
     };
     // One tile; false if a wait gave up (the abort flag is raised then).
     auto tile = [&](int j) -> bool {
       const int b = j & 1;
       if (!__all_sync(0xffffffffu,
-                      mbar_spin(smem_u32(&bars.s_done[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 20 + wg)))
+                      mbar_spin(smem_u32(&bars.s_done[j % kKStages]), (j / kKStages) & 1, abort_flag, p.err, 20 + wg,
+                                kLimit)))
         return false;
       tc_fence_after();
       // Copy this half's 64 scores to registers; P_j is later written over their first 32 columns.
@@ -636,7 +648,7 @@ bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* 
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool COUNT>
+template <int D, bool COUNT, bool PROBE = false>
 cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k, const void* v, int n_keys,
                          int hq, int hkv, float scale, void* out, const AttentionDiag& diag, int32_t* err,
                          cudaStream_t s) {
@@ -675,10 +687,10 @@ cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k
   size_t smem = 1024 + (size_t)(kBM + (kKStages + kVStages) * kBN) * D * 2;
   if (smem < 117 * 1024) smem = 117 * 1024;  // one CTA per SM: the CTA takes all 512 TMEM columns
   static std::atomic<uint64_t> configured{0};
-  const cudaError_t e = set_smem_limit_once(hkvd_attention_kernel<D, COUNT>, (int)smem, configured);
+  const cudaError_t e = set_smem_limit_once(hkvd_attention_kernel<D, COUNT, PROBE>, (int)smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_pdl(hkvd_attention_kernel<D, COUNT>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map, tv_map,
-                    to_map, p);
+  return launch_pdl(hkvd_attention_kernel<D, COUNT, PROBE>, n_qtiles * hkv, kThreads, smem, s, tq_map, tk_map,
+                    tv_map, to_map, p);
 }
 
 }  // namespace
@@ -695,6 +707,13 @@ cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, 
     return count ? launch_typed<64, true>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s)
                  : launch_typed<64, false>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_timeout_probe(const void* q, QueryPositions qp, int32_t mq, const void* k,
+                                           const void* v, int32_t n_keys, int32_t hq, int32_t hkv, float scale,
+                                           void* out, int32_t* err, cudaStream_t s) {
+  if (mq <= 0 || n_keys <= kBN) return cudaErrorInvalidValue;
+  return launch_typed<128, false, true>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, AttentionDiag(), err, s);
 }
 
 }  // namespace cb

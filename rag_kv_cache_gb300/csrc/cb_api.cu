@@ -8,6 +8,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/cacheblend.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -35,6 +37,14 @@ struct cb_plan {
 };
 
 namespace {
+
+// Every entry point is one NVTX range named after it, so a profile of a request reads by call
+// (a push and a pop through an unset function pointer when no tool collects NVTX).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define CB_NVTX_RANGE() const NvtxRange cb_nvtx_range_(__func__)
 
 thread_local std::string g_last_error = "no error";
 
@@ -96,6 +106,7 @@ int32_t cb_version(void) { return 100; }
 const char* cb_last_error_string(void) { return g_last_error.c_str(); }
 
 cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
+  CB_NVTX_RANGE();
   CB_TRY(need_ptr(cfg, "cfg"));
   CB_TRY(need_ptr(out, "out"));
   *out = nullptr;
@@ -173,6 +184,7 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
 }
 
 cb_status cb_plan_destroy(cb_plan* plan) {
+  CB_NVTX_RANGE();
   if (plan == nullptr) return CB_OK;
   cudaDeviceSynchronize();
   cudaFree(plan->rope_tab);
@@ -216,6 +228,7 @@ cb_status cb_layer_sizes(const cb_plan* plan, int32_t layer, int32_t* n_cand, in
 cb_status cb_rope_rerotate(cb_plan* plan, void* out, const void* x, const int32_t* in_rows,
                            const int32_t* out_rows, const int32_t* pos_from, const int32_t* pos_to, int32_t n,
                            int32_t n_heads, int32_t x_rows, int32_t out_rows_total, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (n < 0 || n_heads <= 0 || x_rows < 0 || out_rows_total < 0)
     return fail(CB_ERR_INVALID_ARG, "negative size or n_heads <= 0");
@@ -235,6 +248,7 @@ cb_status cb_rope_rerotate(cb_plan* plan, void* out, const void* x, const int32_
 
 cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
                           float* dev, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (m < 0) return fail(CB_ERR_INVALID_ARG, "m < 0");
   if (m == 0) return CB_OK;
@@ -250,6 +264,7 @@ cb_status cb_kv_deviation(cb_plan* plan, const void* v_new, const void* v_old, c
 
 cb_status cb_kv_deviation_kv(cb_plan* plan, const void* k_new, const void* k_old, const void* v_new,
                              const void* v_old, const int32_t* cand, int32_t m, float* dev, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (m < 0) return fail(CB_ERR_INVALID_ARG, "m < 0");
   if (m == 0) return CB_OK;
@@ -268,6 +283,7 @@ cb_status cb_kv_deviation_kv(cb_plan* plan, const void* k_new, const void* k_old
 
 cb_status cb_hkvd_topk(cb_plan* plan, const float* dev, const int32_t* cand, int32_t m, int32_t k,
                        int32_t* sel_tok, int32_t* sel_row, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (m < 0 || k < 0 || k > m) return fail(CB_ERR_INVALID_ARG, "need 0 <= k <= m (k=%d, m=%d)", k, m);
   if (k == 0) return CB_OK;
@@ -281,6 +297,7 @@ cb_status cb_hkvd_topk(cb_plan* plan, const float* dev, const int32_t* cand, int
 
 cb_status cb_fuse_scatter(cb_plan* plan, void* k_fused, void* v_fused, const void* k_new, const void* v_new,
                           const int32_t* sel_tok, int32_t k, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (k < 0 || k > plan->n_ctx) return fail(CB_ERR_INVALID_ARG, "need 0 <= k <= n_ctx");
   if (k + plan->cfg.n_suffix == 0) return CB_OK;
@@ -298,6 +315,7 @@ cb_status cb_fuse_scatter(cb_plan* plan, void* k_fused, void* v_fused, const voi
 
 cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
                             const void* v, int32_t n_keys, float scale, void* out, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (mq < 0 || n_keys < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
   if (mq == 0) return CB_OK;
@@ -315,9 +333,28 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                      "cb_hkvd_attention");
 }
 
+cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq,
+                                         const void* k, const void* v, int32_t n_keys, void* out, void* stream) {
+  CB_NVTX_RANGE();
+  CB_TRY(check_plan(plan));
+  if (plan->cfg.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "the wait-timeout probe needs head_dim 128");
+  if (mq <= 0 || n_keys <= 128) return fail(CB_ERR_INVALID_ARG, "the wait-timeout probe needs mq > 0, n_keys > 128");
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_ptr(q_pos, "q_pos"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  CB_TRY(need_tensor(out, "out"));
+  const cb::QueryPositions qp{q_pos, mq, 0, true};
+  return cuda_status(cb::launch_attention_timeout_probe(q, qp, mq, k, v, n_keys, plan->cfg.hq, plan->cfg.hkv,
+                                                        1.0f / std::sqrt(128.0f), out, plan->err,
+                                                        static_cast<cudaStream_t>(stream)),
+                     "cb_test_attention_wait_timeout");
+}
+
 cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
                                 const void* v, int32_t n_keys, float scale, float eps, void* out, void* row_stats,
                                 int32_t* counts, uint64_t* total, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (mq < 0 || n_keys < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
   if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(CB_ERR_INVALID_ARG, "eps must be positive and finite");
@@ -353,6 +390,7 @@ cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_p
 
 cb_status cb_output_deviation(cb_plan* plan, const void* o, const void* o_ref, int32_t rows, double* sums,
                               void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (rows < 0) return fail(CB_ERR_INVALID_ARG, "rows < 0");
   CB_TRY(need_ptr(sums, "sums"));
@@ -368,6 +406,7 @@ cb_status cb_output_deviation(cb_plan* plan, const void* o, const void* o_ref, i
 cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows,
                             int32_t m, const void* w_qkv, int32_t encode, void* x_gathered, void* q, void* k, void* v,
                             void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (m < 0 || x_rows < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
   if (m == 0) return CB_OK;
@@ -390,6 +429,7 @@ cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_
 
 cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
                               float scale, void* out, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (n_keys < 0) return fail(CB_ERR_INVALID_ARG, "n_keys < 0");
   if (n_keys == 0) return CB_OK;
@@ -482,6 +522,7 @@ static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* 
 }
 
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   LayerShape sh;
   CB_TRY(validate_io(plan, layer, io, io ? io->cand : nullptr, &sh));
@@ -492,6 +533,7 @@ cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, vo
 }
 
 cb_status cb_blend_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, int32_t stage, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (stage < CB_STAGE_DEVIATION || stage > CB_STAGE_ATTENTION) return fail(CB_ERR_INVALID_ARG, "unknown stage %d", stage);
   LayerShape sh;
@@ -500,6 +542,7 @@ cb_status cb_blend_stage(cb_plan* plan, int32_t layer, const cb_layer_io* io, in
 }
 
 cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios, void* stream) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   if (n_layers < 1) return fail(CB_ERR_INVALID_ARG, "n_layers must be >= 1");
   CB_TRY(need_ptr(ios, "ios"));
@@ -541,6 +584,7 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
 }
 
 cb_status cb_check(cb_plan* plan) {
+  CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
   int32_t h[2] = {0, -1};
   cudaError_t e = cudaDeviceSynchronize();

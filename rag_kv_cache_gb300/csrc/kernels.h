@@ -85,6 +85,13 @@ cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, 
                                   float scale, void* out, int32_t* err, cudaStream_t s,
                                   const AttentionDiag& diag = AttentionDiag());
 
+// The attention kernel's wait-timeout probe (test support): the same launch with head_dim 128,
+// in the kernel instance whose K producer never requests key tile 1 and whose waits give up
+// after 100 us. Needs n_keys > 128 (a second key tile).
+cudaError_t launch_attention_timeout_probe(const void* q, QueryPositions qp, int32_t mq, const void* k,
+                                           const void* v, int32_t n_keys, int32_t hq, int32_t hkv, float scale,
+                                           void* out, int32_t* err, cudaStream_t s);
+
 // Diagnostics reductions. sum_counts: *total = sum of counts[0..n) (64-bit). output_deviation:
 // sums[0] = sum (a - b)^2, sums[1] = sum b^2 over n bf16 elements, in fp64 (order of the block
 // partials not fixed: the last bits may differ between runs).

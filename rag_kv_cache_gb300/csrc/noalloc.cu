@@ -10,6 +10,7 @@
 // deviations (the only intermediate) in a fixed array compiled into the
 // library instead of a buffer someone has to allocate.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 
@@ -93,11 +94,9 @@ cudaError_t scratch_on_current_device(float** out) {
   return cudaSuccess;
 }
 
-}  // namespace
-
-extern "C" cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
-                                            int32_t k, int32_t n_rows, int32_t hkv, int32_t head_dim,
-                                            int32_t* sel_tok, int32_t* sel_row, void* stream) {
+cb_status select_noalloc(const void* v_new, const void* v_old, const int32_t* cand, int32_t m, int32_t k,
+                         int32_t n_rows, int32_t hkv, int32_t head_dim, int32_t* sel_tok, int32_t* sel_row,
+                         void* stream) {
   if (m < 0 || k < 0 || k > m) return noalloc_fail(CB_ERR_INVALID_ARG, "need 0 <= k <= m");
   if (m > CB_NOALLOC_MAX_CANDIDATES)
     return noalloc_fail(CB_ERR_INVALID_ARG,
@@ -118,4 +117,15 @@ extern "C" cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old
   if (e == cudaSuccess) e = cb::launch_hkvd_topk(scratch, cand, m, k, sel_tok, sel_row, nullptr, s);
   if (e != cudaSuccess) return noalloc_fail(CB_ERR_CUDA, cudaGetErrorString(e));
   return CB_OK;
+}
+
+}  // namespace
+
+extern "C" cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int32_t* cand, int32_t m,
+                                            int32_t k, int32_t n_rows, int32_t hkv, int32_t head_dim,
+                                            int32_t* sel_tok, int32_t* sel_row, void* stream) {
+  nvtxRangePushA("cb_hkvd_select_noalloc");  // one NVTX range per entry point, as in cb_api.cu
+  const cb_status st = select_noalloc(v_new, v_old, cand, m, k, n_rows, hkv, head_dim, sel_tok, sel_row, stream);
+  nvtxRangePop();
+  return st;
 }

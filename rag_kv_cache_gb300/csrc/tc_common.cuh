@@ -11,6 +11,7 @@ namespace cb {
 namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
+constexpr unsigned long long kProbeTimeoutNs = 100000ull;  // the wait-timeout probe's limit: 100 us
 constexpr uint32_t kSuspendHintNs = 200000;  // a sleeping waiter re-checks abort and time at least this often
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -60,7 +61,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // Slow path of mbar_wait: sleep-wait with a time limit. A few plain try_waits come first: reading
 // %globaltimer takes hundreds of cycles, so the clock for the limit starts only for a long wait.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                            int site, bool honour_abort) {
+                                            int site, bool honour_abort, uint64_t limit_ns) {
   for (int n = 0; n < 16; ++n)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer();
@@ -68,7 +69,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if ((n & 7u) == 0) {
       if (honour_abort && *abort_flag) return false;
-      if (global_timer() - t0 > kTimeoutNs) {
+      if (global_timer() - t0 > limit_ns) {
         *abort_flag = 1;
         record_error(err, kErrTimeout, site);
         return false;
@@ -94,7 +95,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // resumes several hundred cycles after the phase completes, a polling one within tens.
 // Same limit and abort behaviour as mbar_wait.
 __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                            int site) {
+                                            int site, uint64_t limit_ns) {
   // Poll without the clock first (reading %globaltimer takes hundreds of cycles and would delay
   // noticing a phase that completes within the first few polls); then with the time limit.
   for (int n = 0; n < 512; ++n)
@@ -104,7 +105,7 @@ __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volat
     if (mbar_test(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer() - t0 > kTimeoutNs) {
+      if (global_timer() - t0 > limit_ns) {
         *abort_flag = 1;
         record_error(err, kErrTimeout, site);
         return false;
@@ -114,16 +115,16 @@ __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volat
 }
 
 __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                          int site) {
+                                          int site, uint64_t limit_ns = kTimeoutNs) {
   if (mbar_test(bar, parity)) return true;
-  return mbar_spin_slow(bar, parity, abort_flag, err, site);
+  return mbar_spin_slow(bar, parity, abort_flag, err, site, limit_ns);
 }
 
 // Wait for the phase of parity `parity` to complete; false on abort or timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                          int site, bool honour_abort = true) {
+                                          int site, bool honour_abort = true, uint64_t limit_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err, site, honour_abort);
+  return mbar_wait_slow(bar, parity, abort_flag, err, site, honour_abort, limit_ns);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,

@@ -59,3 +59,30 @@ def assert_close_attention(got, ref, vscale, what="attention"):
     bad = err > lim
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; "
                            f"max abs err {err.max():.3e}; max err/limit {(err / lim).max():.3f}")
+
+
+# Attention elements measured against the fixed bf16 bound |got - ref| <= 2e-2 + 1e-2 |ref|
+# (without the widening by sum_j p_j |v_j| above), per compared case. Written as JSON to the
+# path in CB_PARITY_REPORT at the end of the session, when that variable is set.
+STRICT_ATTENTION = []
+
+
+def record_strict_attention(what, got, ref):
+    import numpy as np
+
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    lim = 2e-2 + 1e-2 * np.abs(ref)
+    STRICT_ATTENTION.append({"case": what, "elements": int(err.size), "outside_fixed_bound": int((err > lim).sum()),
+                             "max_err_over_limit": float((err / lim).max()) if err.size else 0.0,
+                             "max_abs_err": float(err.max()) if err.size else 0.0})
+
+
+def pytest_sessionfinish(session, exitstatus):
+    path = os.environ.get("CB_PARITY_REPORT")
+    if path and STRICT_ATTENTION:
+        import json
+
+        with open(path, "w") as f:
+            json.dump(STRICT_ATTENTION, f, indent=1)

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import assert_close_attention, assert_close_bf16
+from conftest import assert_close_attention, assert_close_bf16, record_strict_attention
 from oracle.blend import blend_layer, candidate_layer, gradual_filter_schedule
 from oracle.deviation import bf16_bits_to_f64
 from workloads import get_config
@@ -49,25 +49,79 @@ def run_gpu_layers(cb, cfg, layers, style="half", r1=None, r2=None, deviation="v
     return results
 
 
-def oracle_layers(cfg, layers, style="half", attention_rows=None, deviation="v", filter="keep"):
-    """The oracle's blend for the requested layers (selection chain followed from layer 1)."""
+def oracle_layers(cfg, layers, style="half", attention_rows=None, deviation="v", filter="keep", full_rows=()):
+    """The oracle's blend for the requested layers (selection chain followed from layer 1).
+
+    Layers that are not requested only carry the chain forward: a layer that keeps its
+    candidates passes them on unchanged, one that selects runs only its deviation and top-k.
+    attention_rows(mq, layer) picks the query rows whose attention the oracle computes; layers
+    in full_rows compute every row."""
+    from oracle.deviation import deviation_canonical_f32, kv_deviation_canonical_f32
+    from oracle.positions import chunk_local_positions
+    from oracle.topk import hkvd_topk
+
     sets = hkvd_noise_sets(cfg)
     sched = gradual_filter_schedule(cfg.n_ctx, cfg.layers, cfg.r1_pct, cfg.r2_pct, filter)
+    p_old = chunk_local_positions(cfg.n_chunks, cfg.chunk_len)
     sels = {0: np.arange(cfg.n_ctx)}
     out = {}
     for layer, k, selects in sched[: max(layers)]:
-        inp = generate_layer(cfg, layer, sets)
-        want = layer in layers
-        rows = attention_rows(k + cfg.n_suffix, layer) if (want and attention_rows) else None
-        res = blend_layer(cfg, inp, layer, sels[candidate_layer(layer, filter)], k, selects, style,
-                          attention_rows=(rows if want else False), deviation=deviation)
-        if want:
+        cand = sels[candidate_layer(layer, filter)]
+        if layer in layers:
+            inp = generate_layer(cfg, layer, sets)
+            rows = None if (layer in full_rows or attention_rows is None) else attention_rows(k + cfg.n_suffix, layer)
+            res = blend_layer(cfg, inp, layer, cand, k, selects, style, attention_rows=rows, deviation=deviation)
             out[layer] = res
-        sels[layer] = res.sel_tok
+            sels[layer] = res.sel_tok
+        elif selects:
+            inp = generate_layer(cfg, layer, sets)
+            if deviation == "kv":
+                dev = kv_deviation_canonical_f32(inp.k_new[cand], inp.k_old[cand], inp.v_new[cand], inp.v_old[cand],
+                                                 p_old[cand], cfg.rope_theta, style)
+            else:
+                dev = deviation_canonical_f32(inp.v_new[cand], inp.v_old[cand])
+            sels[layer], _ = hkvd_topk(dev, cand, k)
+        else:
+            sels[layer] = cand
     return out
 
 
-def compare(g, o, cfg, rows=None):
+def run_gpu_request(cb, cfg, layers, deviation="v", filter="keep"):
+    """All layers of the request in one cb_blend_request call; {layer: outputs} for the requested
+    layers. Inputs are generated on the host cores in parallel and moved to the device at once."""
+    import bench
+
+    plan = cb.Plan.from_config(cfg, deviation=deviation, filter=filter)
+    sets = hkvd_noise_sets(cfg)
+    keep = {}
+
+    def to_device(inp):
+        if inp.layer in layers:
+            keep[inp.layer] = inp
+        return layer_tensors(inp)
+
+    d_in = bench.generate_inputs(cfg, list(range(1, cfg.layers + 1)), sets, consume=to_device)
+    bufs = [cb.LayerBuffers(plan) for _ in range(cfg.layers)]
+    cb.cb_blend_request(plan, [dict(bufs=bufs[i], **d_in[i]) for i in range(cfg.layers)])
+    torch.cuda.synchronize()
+    plan.check()
+    results = {}
+    for layer in layers:
+        b = bufs[layer - 1]
+        n_cand, k, mq, selects = plan.layer_sizes(layer)
+        results[layer] = dict(
+            inp=keep[layer], k=k, mq=mq, selects=selects,
+            dev=b.dev[:n_cand].cpu().numpy().copy() if selects else None,
+            sel_tok=b.sel_tok[:k].cpu().numpy().copy(), sel_row=b.sel_row[:k].cpu().numpy().copy(),
+            k_fused=bf16_bits(b.k_fused), v_fused=bf16_bits(b.v_fused),
+            q_rot=bf16_bits(b.q_rot[:mq]), out=bf16_bits(b.out[:mq]))
+    plan.close()
+    del d_in, bufs
+    torch.cuda.empty_cache()
+    return results
+
+
+def compare(g, o, cfg, rows=None, what=""):
     assert np.array_equal(g["sel_tok"], o.sel_tok)
     assert np.array_equal(g["sel_row"], o.sel_row)
     if o.dev is not None:
@@ -77,9 +131,20 @@ def compare(g, o, cfg, rows=None):
     assert_close_bf16(bf16_bits_to_f64(g["q_rot"]), o.q_rot, what="encoded Q")
     got = bf16_bits_to_f64(g["out"])
     if rows is None:
-        assert_close_attention(got, o.out, o.out_vscale)
-    else:
-        assert_close_attention(got[rows], o.out[rows], o.out_vscale[rows], what="attention (sampled rows)")
+        rows = np.arange(got.shape[0])
+    record_strict_attention(what or cfg.name, got[rows], o.out[rows])
+    assert_close_attention(got[rows], o.out[rows], o.out_vscale[rows], what=f"attention ({rows.size} rows)")
+
+
+def sampled_rows(cfg, seed, n=256):
+    """n seeded query rows plus the first and last HKVD rows and the first and last suffix rows."""
+    rng = np.random.default_rng(seed)
+
+    def pick(mq, layer):
+        k = mq - cfg.n_suffix
+        fixed = [0, mq - 1] + ([k - 1] if k > 0 else []) + ([k] if cfg.n_suffix > 0 else [])
+        return np.unique(np.concatenate([np.asarray(fixed), rng.choice(mq, size=min(mq, n), replace=False)]))
+    return pick
 
 
 @pytest.mark.parametrize("style", ["half", "interleaved"])
@@ -98,7 +163,7 @@ def test_small_multilayer_gradual_filter(cb):
     g = run_gpu_layers(cb, cfg, [1, 2, 3, 4, 5])
     o = oracle_layers(cfg, [1, 2, 3, 4, 5])
     for layer in range(1, 6):
-        compare(g[layer], o[layer], cfg)
+        compare(g[layer], o[layer], cfg, what=f"small5 layer {layer}")
     assert np.array_equal(g[4]["sel_tok"], g[2]["sel_tok"])
 
 
@@ -122,24 +187,25 @@ def test_ratio_sweep(cb, r):
     pick = lambda mq, layer: np.sort(rng.choice(mq, size=min(mq, 192), replace=False))
     g = run_gpu_layers(cb, cfg, [1])[1]
     o = oracle_layers(cfg, [1], attention_rows=pick)[1]
-    compare(g, o, cfg, rows=np.flatnonzero(~np.isnan(o.out[:, 0, 0])))
+    compare(g, o, cfg, rows=np.flatnonzero(~np.isnan(o.out[:, 0, 0])), what=f"sweep r={r}%")
     if r == 100:
         assert g["sel_tok"].tolist() == list(range(cfg.n_ctx))
 
 
-@pytest.mark.parametrize("name,layers", [("mistral7b", [1, 2, 3]), ("llama70b", [1, 2, 3]), ("long32k", [1])])
-def test_full_size_workloads(cb, name, layers):
+@pytest.mark.parametrize("name,layers,full_rows", [("mistral7b", [1, 2, 3, 32], [3]), ("llama70b", [1, 2, 3, 80], []),
+                                                ("long32k", [1, 2, 3, 32], [])])
+def test_full_size_requests(cb, name, layers, full_rows):
+    # every layer of the request through cb_blend_request (the selection chain on the device);
+    # the oracle checks the first three layers and the last: sets, rows, deviations and fused V
+    # bit for bit, K, queries and >= 256 seeded attention rows (plus the first and last HKVD and
+    # suffix rows) within tolerance; the layers in full_rows check every attention row
     cfg = get_config(name)
-    rng = np.random.default_rng(cfg.config_id)
-    # sampled rows: the first and last query rows, the suffix's first row, and a seeded spread
-    def pick(mq, layer):
-        k = mq - cfg.n_suffix
-        fixed = np.array([0, k - 1, k, mq - 1]) if k > 0 else np.array([0, mq - 1])
-        return np.unique(np.concatenate([fixed, rng.choice(mq, size=min(mq, 60), replace=False)]))
-    g = run_gpu_layers(cb, cfg, layers)
-    o = oracle_layers(cfg, layers, attention_rows=pick)
+    g = run_gpu_request(cb, cfg, layers)
+    o = oracle_layers(cfg, layers, attention_rows=sampled_rows(cfg, cfg.config_id), full_rows=full_rows)
     for layer in layers:
-        compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])))
+        compare(g[layer], o[layer], cfg, rows=np.flatnonzero(~np.isnan(o[layer].out[:, 0, 0])),
+                what=f"{name} layer {layer}")
+    assert np.array_equal(g[layers[-1]]["sel_tok"], g[2]["sel_tok"])  # kept from layer 3 on
 
 
 def test_full_size_kv_reselect(cb):

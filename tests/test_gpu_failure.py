@@ -1,0 +1,58 @@
+"""The attention kernel's failure path: a bounded wait that runs out is reported, and the
+device stays usable.
+
+cb_test_attention_wait_timeout runs the attention kernel in a form whose K-tile producer never
+requests key tile 1 and whose waits give up after 100 us (a barrier that nothing completes, no
+fault, trap or endless loop). Every CTA whose queries reach that tile must record CB_ERR_TIMEOUT
+in the plan's error word, drain what it started, free its tensor memory and return; a normal
+attention call right after must then give the oracle's result on the same SMs.
+"""
+
+import dataclasses
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_close_bf16
+from oracle.attention import causal_gqa_attention
+from oracle.deviation import bf16_bits_to_f64
+from workloads import get_config
+from workloads.generator import f32_to_bf16_bits
+from workloads.torch_io import bf16_bits, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def test_attention_wait_timeout_is_reported_and_the_device_stays_usable(cb):
+    hq, hkv, d, n_keys = 32, 8, 128, 640
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1, chunk_len=n_keys - 1,
+                              n_suffix=1)
+    plan = cb.Plan.from_config(cfg)
+    rng = np.random.default_rng(404)
+    q_pos = np.sort(rng.choice(np.arange(128, n_keys), size=96, replace=False))  # every tile reaches key tile 1
+    mq = q_pos.size
+    q = f32_to_bf16_bits(rng.standard_normal((mq, hq, d)).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    dq, dk, dv = bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+    pos = torch.as_tensor(q_pos.astype(np.int32)).cuda()
+    out = torch.zeros((mq, hq, d), dtype=torch.bfloat16, device="cuda")
+    ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    for _ in range(2):  # the failure and the recovery, twice in a row
+        t0 = time.perf_counter()
+        cb.cb_test_attention_wait_timeout(plan, dq, pos, mq, dk, dv, n_keys, out)
+        with pytest.raises(cb.CacheBlendError) as e:
+            plan.check()  # synchronises: the kernel has returned
+        assert e.value.status == 4 and "flags 0x8 " in str(e.value)
+        assert time.perf_counter() - t0 < 30.0
+        plan.check()  # the error word was read and cleared
+        out.zero_()
+        cb.cb_hkvd_attention(plan, dq, pos, mq, dk, dv, n_keys, out)
+        plan.check()
+        assert_close_bf16(bf16_bits_to_f64(bf16_bits(out)), ref, what="attention after a timed-out launch")
+    with pytest.raises(cb.CacheBlendError) as e:
+        cb.cb_test_attention_wait_timeout(plan, dq, pos, mq, dk, dv, 128, out)  # no key tile 1 to miss
+    assert e.value.status == 1
+    plan.close()
