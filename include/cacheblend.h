@@ -332,6 +332,14 @@ cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int
                                  int32_t k, int32_t n_rows, int32_t hkv, int32_t head_dim,
                                  int32_t* sel_tok, int32_t* sel_row, void* stream);
 
+/* Which of the two attention kernels a cb_hkvd_attention call (or a blend
+ * layer's attention) of mq query rows runs on the plan's device: 1 for the
+ * paired-tile kernel (two 128-row query tiles per CTA whose softmax and
+ * tensor-core work alternate; head_dim 128, and only when the launch fills
+ * at least two waves of the GPU's SMs), 0 for the one-tile kernel. Both
+ * compute the same attention; the answer is for profiling and tests. */
+int32_t cb_attention_uses_paired_tiles(const cb_plan* plan, int32_t mq);
+
 /* Test support for the failure path, not part of the blend (the pages have
  * no counterpart). Runs cb_hkvd_attention's kernel (head_dim 128 only) in a
  * form whose K-tile producer never requests key tile 1 and whose bounded

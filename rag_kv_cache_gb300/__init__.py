@@ -18,7 +18,8 @@ from ._lib import CacheBlendError, check
 __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk",
            "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_attention_sparsity",
            "cb_output_deviation", "cb_qkv_projection", "cb_blend_layer", "cb_blend_stage",
-           "cb_blend_request", "cb_hkvd_select_noalloc", "cb_test_attention_wait_timeout", "cb_check", "cb_version",
+           "cb_blend_request", "cb_hkvd_select_noalloc", "cb_attention_uses_paired_tiles",
+           "cb_test_attention_wait_timeout", "cb_check", "cb_version",
            "LayerBuffers"]
 
 
@@ -194,6 +195,11 @@ def cb_hkvd_select_noalloc(v_new, v_old, cand, m, k, n_rows, sel_tok, sel_row, s
         _ptr(v_new, torch.bfloat16, "v_new"), _ptr(v_old, torch.bfloat16, "v_old"),
         _ptr(cand, torch.int32, "cand"), m, k, n_rows, v_new.shape[1], v_new.shape[2],
         _ptr(sel_tok, torch.int32, "sel_tok"), _ptr(sel_row, torch.int32, "sel_row"), _stream(stream)))
+
+
+def cb_attention_uses_paired_tiles(plan, mq) -> bool:
+    """True if an attention call of mq query rows runs the paired-tile kernel (see cacheblend.h)."""
+    return bool(_lib.load().cb_attention_uses_paired_tiles(plan.handle, mq))
 
 
 def cb_test_attention_wait_timeout(plan, q, q_pos, mq, k, v, n_keys, out, stream=None):

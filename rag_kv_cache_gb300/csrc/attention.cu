@@ -52,6 +52,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "attn_common.cuh"
 #include "tc_common.cuh"
 #include "tmem_ops.cuh"
 
@@ -122,38 +123,6 @@ struct Params {
   float log2_eps;
   int32_t* counts;
 };
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Packed fp32 pairs (sm_100 family f32x2 arithmetic: two lanes per instruction).
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // PROBE: the wait-timeout probe (test support only): the K producer never requests key tile 1
 // and every wait gives up after kProbeTimeoutNs, so the CTA takes its failure path (timeout
@@ -624,30 +593,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                const cuuint32_t* box) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
-                         es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int D, bool COUNT, bool PROBE = false>
 cudaError_t launch_typed(const void* q, QueryPositions qp, int mq, const void* k, const void* v, int n_keys,
                          int hq, int hkv, float scale, void* out, const AttentionDiag& diag, int32_t* err,
@@ -700,6 +645,10 @@ cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, 
                                   int32_t* err, cudaStream_t s, const AttentionDiag& diag) {
   if (mq <= 0) return cudaSuccess;
   const bool count = diag.counts != nullptr;
+  if (!count && diag.row_stats == nullptr && attention_pp_eligible(mq, hq, hkv, head_dim)) {
+    const cudaError_t e = launch_hkvd_attention_pp(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, err, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (head_dim == 128)
     return count ? launch_typed<128, true>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s)
                  : launch_typed<128, false>(q, qp, mq, k, v, n_keys, hq, hkv, scale, out, diag, err, s);

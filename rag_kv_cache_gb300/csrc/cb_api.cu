@@ -333,6 +333,11 @@ cb_status cb_hkvd_attention(cb_plan* plan, const void* q, const int32_t* q_pos, 
                      "cb_hkvd_attention");
 }
 
+int32_t cb_attention_uses_paired_tiles(const cb_plan* plan, int32_t mq) {
+  if (plan == nullptr) return 0;
+  return cb::attention_pp_eligible(mq, plan->cfg.hq, plan->cfg.hkv, plan->cfg.head_dim) ? 1 : 0;
+}
+
 cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq,
                                          const void* k, const void* v, int32_t n_keys, void* out, void* stream) {
   CB_NVTX_RANGE();

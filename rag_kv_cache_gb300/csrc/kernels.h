@@ -85,6 +85,15 @@ cudaError_t launch_hkvd_attention(const void* q, QueryPositions qp, int32_t mq, 
                                   float scale, void* out, int32_t* err, cudaStream_t s,
                                   const AttentionDiag& diag = AttentionDiag());
 
+// The two-query-tile ("ping-pong") attention kernel for large launches (attention_pp.cu):
+// eligible when head_dim is 128 and the launch makes at least two waves of its 256-row CTAs;
+// launch_hkvd_attention picks it then. Returns cudaErrorNotSupported, launching nothing, when
+// the kernel was built with fewer registers than its warpgroups' split needs.
+bool attention_pp_eligible(int32_t mq, int32_t hq, int32_t hkv, int32_t head_dim);
+cudaError_t launch_hkvd_attention_pp(const void* q, QueryPositions qp, int32_t mq, const void* k, const void* v,
+                                     int32_t n_keys, int32_t hq, int32_t hkv, float scale, void* out, int32_t* err,
+                                     cudaStream_t s);
+
 // The attention kernel's wait-timeout probe (test support): the same launch with head_dim 128,
 // in the kernel instance whose K producer never requests key tile 1 and whose waits give up
 // after 100 us. Needs n_keys > 128 (a second key tile).

@@ -60,8 +60,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Slow path of mbar_wait: sleep-wait with a time limit. A few plain try_waits come first: reading
 // %globaltimer takes hundreds of cycles, so the clock for the limit starts only for a long wait.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                            int site, bool honour_abort, uint64_t limit_ns) {
+// The body is force-inlined for kernels whose warpgroups change their register counts
+// (setmaxnreg), where a call to an out-of-line function cannot be register-allocated.
+__device__ __forceinline__ bool mbar_wait_slow_body(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                    int32_t* err, int site, bool honour_abort, uint64_t limit_ns) {
   for (int n = 0; n < 16; ++n)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer();
@@ -76,6 +78,11 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
       }
     }
   }
+}
+
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                            int site, bool honour_abort, uint64_t limit_ns) {
+  return mbar_wait_slow_body(bar, parity, abort_flag, err, site, honour_abort, limit_ns);
 }
 
 // Non-blocking test: true once the phase of parity `parity` has completed.
@@ -93,11 +100,11 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // Busy-wait for the waits on the tile loop's critical path: a thread suspended in try_wait
 // resumes several hundred cycles after the phase completes, a polling one within tens.
-// Same limit and abort behaviour as mbar_wait.
-__device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                            int site, uint64_t limit_ns) {
-  // Poll without the clock first (reading %globaltimer takes hundreds of cycles and would delay
-  // noticing a phase that completes within the first few polls); then with the time limit.
+// Same limit and abort behaviour as mbar_wait. Poll without the clock first (reading
+// %globaltimer takes hundreds of cycles and would delay noticing a phase that completes within
+// the first few polls); then with the time limit.
+__device__ __forceinline__ bool mbar_spin_slow_body(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                    int32_t* err, int site, uint64_t limit_ns) {
   for (int n = 0; n < 512; ++n)
     if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer();
@@ -114,10 +121,27 @@ __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volat
   }
 }
 
+__device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                            int site, uint64_t limit_ns) {
+  return mbar_spin_slow_body(bar, parity, abort_flag, err, site, limit_ns);
+}
+
 __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                           int site, uint64_t limit_ns = kTimeoutNs) {
   if (mbar_test(bar, parity)) return true;
   return mbar_spin_slow(bar, parity, abort_flag, err, site, limit_ns);
+}
+
+// The same waits with the slow paths inlined (for kernels that use setmaxnreg).
+__device__ __forceinline__ bool mbar_spin_inl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                              int site, uint64_t limit_ns = kTimeoutNs) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_spin_slow_body(bar, parity, abort_flag, err, site, limit_ns);
+}
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                              int site, bool honour_abort = true, uint64_t limit_ns = kTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_body(bar, parity, abort_flag, err, site, honour_abort, limit_ns);
 }
 
 // Wait for the phase of parity `parity` to complete; false on abort or timeout.

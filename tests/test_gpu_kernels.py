@@ -381,3 +381,51 @@ def test_attention_tiles_mixing_early_and_late_rows(cb, hq, hkv, d):
     assert np.array_equal(outs[0], outs[1])
     ref = causal_gqa_attention(bf16_bits_to_f64(q), q_pos, bf16_bits_to_f64(k), bf16_bits_to_f64(v))
     assert_close_bf16(bf16_bits_to_f64(outs[0]), ref, what="attention with early and late rows in one tile")
+
+
+# ---------------------------------------------------------------- paired-tile attention (large launches)
+def _attention_sampled(cb, hq, hkv, d, n_keys, q_pos, seed, rows=256, scale_q=1.0, peaked=False):
+    """Attention of len(q_pos) query rows (a launch large enough for the paired-tile kernel),
+    checked against the oracle on `rows` seeded rows plus the first and last rows."""
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=max(n_keys - 1, 1), n_suffix=1)
+    plan = _plan(cb, cfg)
+    mq = len(q_pos)
+    assert cb.cb_attention_uses_paired_tiles(plan, mq)
+    rng = np.random.default_rng(seed)
+    q = f32_to_bf16_bits((scale_q * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    k = rng.standard_normal((n_keys, hkv, d)).astype(np.float32)
+    if peaked:  # a few keys far above the rest, spread over the range: the running max jumps
+        k[rng.choice(n_keys, size=8, replace=False)] *= 6.0
+    k = f32_to_bf16_bits(k)
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    got = bf16_bits_to_f64(bf16_bits(out))
+    assert not np.isnan(got).any()  # every row written, including the ragged last tile
+    pick = np.unique(np.concatenate([[0, mq - 1], rng.choice(mq, size=min(rows, mq), replace=False)]))
+    ref = causal_gqa_attention(bf16_bits_to_f64(q[pick]), np.asarray(q_pos)[pick], bf16_bits_to_f64(k),
+                               bf16_bits_to_f64(v))
+    plan.close()
+    return got[pick], ref
+
+
+@pytest.mark.parametrize("hq,hkv,mq,n_keys", [(32, 8, 2500, 4000),   # odd tile count: the last pair has no tile 1
+                                              (64, 8, 2600, 9000),   # Llama-70B grouping
+                                              (8, 8, 10000, 12000),  # one query head per kv head
+                                              (16, 1, 5500, 6000)])  # sixteen query heads per kv head
+def test_paired_tile_attention_sparse_rows(cb, hq, hkv, mq, n_keys):
+    rng = np.random.default_rng(mq)
+    q_pos = np.sort(rng.choice(n_keys, size=mq, replace=False))
+    got, ref = _attention_sampled(cb, hq, hkv, 128, n_keys, q_pos, seed=hq + mq)
+    assert_close_bf16(got, ref, what=f"paired-tile attention hq={hq} hkv={hkv} mq={mq}")
+
+
+def test_paired_tile_attention_dense_suffix_and_rescale(cb):
+    # every position from 0 (causal diagonal in every key tile), keys that force the running max
+    # up by more than 2^8 inside the loop
+    n_keys = 3000
+    q_pos = np.arange(n_keys)
+    got, ref = _attention_sampled(cb, 32, 8, 128, n_keys, q_pos, seed=7, scale_q=2.0, peaked=True)
+    assert_close_bf16(got, ref, what="paired-tile attention, all positions, peaked keys")
