@@ -525,14 +525,15 @@ __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
                          head_dim, t.tab + (size_t)tok * (head_dim / 2), false, lane);
     return;
   }
-  // The row's source does not depend on the selection for suffix rows (always recomputed) and
-  // mostly is the cache for context rows: pull those lines into L2 while warp 0 reads the list.
+  // A suffix row's source does not depend on the selection (always recomputed): pull its lines
+  // into L2 while warp 0 reads the list. A context row's source is known only after the list
+  // is read (prefetching the cached row would read a selected row's lines for nothing).
   {
     const int tok = blockIdx.x * kFuseRows + warp;
-    if (tok < n_tokens) {
+    if (tok >= n_ctx && tok < n_tokens) {
       const size_t rb = (size_t)hkv * head_dim * 2;
-      const uint8_t* kp = (tok < n_ctx ? k_old : k_new) + tok * rb;
-      const uint8_t* vp = (tok < n_ctx ? v_old : v_new) + tok * rb;
+      const uint8_t* kp = k_new + tok * rb;
+      const uint8_t* vp = v_new + tok * rb;
       for (size_t off = (size_t)lane * 128; off < rb; off += 32 * 128) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(kp + off));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(vp + off));
