@@ -577,8 +577,11 @@ def run_ours(args, cfg):
     attn_s = stage_ms["attention"] / 1e3
     achieved_tf = float(flops.sum()) / attn_s / 1e12
     peak_tf = peaks["bf16_tflops_sustained"]
-    traffic = traffic_for("attention.cu", cfg.name)
-    roofline = {"kernel": "hkvd_attention", "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
+    # the kernel the request's attention launches run (all layers of a workload take the same one here)
+    paired = cb.cb_attention_uses_paired_tiles(plan, sizes[-1][2])
+    traffic = traffic_for("attention_pp.cu" if paired else "attention.cu", cfg.name)
+    roofline = {"kernel": "hkvd_attention_pp (two query tiles per CTA)" if paired else "hkvd_attention",
+                "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
                 "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                 "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
