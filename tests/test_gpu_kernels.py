@@ -197,7 +197,7 @@ def test_deviation_golden_rounding_cases(cb):
 
 
 # ---------------------------------------------------------------- top-k
-@pytest.mark.parametrize("m", [1, 7, 64, 1000, 1024, 1025, 3072, 32768, 40000])
+@pytest.mark.parametrize("m", [1, 7, 64, 256, 257, 1000, 1024, 1025, 3072, 4096, 4097, 32768, 40000])
 def test_topk_bit_exact_with_ties(cb, m):
     plan = _plan(cb, get_config("tiny"))
     rng = np.random.default_rng(m)
