@@ -324,16 +324,17 @@ def cpu_baseline(cfg, inputs, deviation="v", filter="keep"):
     layer_ids = sampled_layers(cfg)
     chain, sels = oracle_chain(cfg, inputs[:len(layer_ids)], deviation, filter)
     rng = np.random.default_rng(cfg.seed + 17)
-    row_frac = min(1.0, 4096.0 / max(1, cfg.n_ctx))
+    row_frac = min(1.0, 8192.0 / max(1, cfg.n_ctx))
+    n_blocks = 4
     spent, est = 0.0, {}
     for i, layer in enumerate(layer_ids):
-        s, e = oracle_layer_sample(cfg, inputs[i], chain[i], sels[layer], rng, row_frac, 2, deviation)
+        s, e = oracle_layer_sample(cfg, inputs[i], chain[i], sels[layer], rng, row_frac, n_blocks, deviation)
         spent += s
         est[layer] = [e]
     t_step = oracle_step_estimate(cfg, est)
     sample = (f"oracle on seeded samples of layers {', '.join(map(str, layer_ids))} of {cfg.name}: "
               f"{row_frac:.3g} of the rows of deviation, top-k, re-rotation, encoding and fuse (time x "
-              f"{1 / row_frac:.3g}) and 2 of its 256-query-row attention blocks per layer (time x the "
+              f"{1 / row_frac:.3g}) and {n_blocks} of its 256-query-row attention blocks per layer (time x the "
               f"score entries of all blocks / sampled); {spent:.1f} s of CPU work; per-step time "
               f"t1 + t2 + {max(0, cfg.layers - 2)} t3 = {t_step:.1f} s")
     return {"value": cfg.n_ctx * cfg.layers / t_step, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
