@@ -2,6 +2,7 @@
 // checks, the plan (RoPE table, device error word, scratch), and the
 // per-layer driver that enqueues the kernels of one layer on the caller's
 // stream without any host synchronisation.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -526,6 +527,32 @@ static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* 
   }
 }
 
+// The selections of layers 2..n_layers (all from cand = S_1, k_2 each), kSelectBatchMax layers per
+// pair of launches.
+static cb_status enqueue_select_batches(cb_plan* plan, int32_t n_layers, const cb_layer_io* ios,
+                                        const int32_t* cand, const LayerShape& sh, cudaStream_t s) {
+  const auto& c = plan->cfg;
+  const bool kv = c.deviation == CB_DEV_KV;
+  for (int32_t l0 = 2; l0 <= n_layers; l0 += cb::kSelectBatchMax) {
+    cb::SelectBatch b = {};
+    b.n = std::min<int32_t>(cb::kSelectBatchMax, n_layers - l0 + 1);
+    for (int i = 0; i < b.n; ++i) {
+      const cb_layer_io& io = ios[l0 - 1 + i];
+      b.k_new[i] = kv ? io.k_new : nullptr;
+      b.k_old[i] = kv ? io.k_old : nullptr;
+      b.v_new[i] = io.v_new;
+      b.v_old[i] = io.v_old;
+      b.dev[i] = io.dev;
+      b.sel_tok[i] = io.sel_tok;
+      b.sel_row[i] = io.sel_row;
+    }
+    CB_TRY(cuda_status(cb::launch_select_batch(b, cand, sh.n_cand, sh.k, plan->n_ctx, c.hkv, c.head_dim, c.chunk_len,
+                                               c.rope_style, table(plan), plan->err, s),
+                       "batched selection"));
+  }
+  return CB_OK;
+}
+
 cb_status cb_blend_layer(cb_plan* plan, int32_t layer, const cb_layer_io* io, void* stream) {
   CB_NVTX_RANGE();
   CB_TRY(check_plan(plan));
@@ -568,13 +595,23 @@ cb_status cb_blend_request(cb_plan* plan, int32_t n_layers, const cb_layer_io* i
   CB_TRY(cuda_status(cudaStreamWaitEvent(plan->aux_stream, plan->ev_fork, 0), "fork"));
   for (int a = 1; a < kAttnStreams; ++a)
     CB_TRY(cuda_status(cudaStreamWaitEvent(attn_stream[a], plan->ev_fork, 0), "fork"));
+  // Re-selection: every layer >= 2 selects k_2 from the same candidates S_1, so their deviations and
+  // top-k go out as two batched launches right after layer 1's selection (instead of a deviation and
+  // a one-block top-k ahead of every fuse), and the fuses then run ahead of the attention as they do
+  // when the set is kept.
+  const bool batch_select = reselect && n_layers >= 2;
   for (int32_t l = 1; l <= n_layers; ++l) {
     const cb_layer_io* io = &ios[l - 1];
     const int32_t* cand = cand_of(l);
     LayerShape sh;
     CB_TRY(validate_io(plan, l, io, cand, &sh));
-    for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_FUSE; ++st)
-      CB_TRY(enqueue_stage(plan, l, io, cand, sh, st, plan->aux_stream));
+    if (batch_select && l >= 2) {
+      if (l == 2) CB_TRY(enqueue_select_batches(plan, n_layers, ios, ios[0].sel_tok, sh, plan->aux_stream));
+      CB_TRY(enqueue_stage(plan, l, io, cand, sh, CB_STAGE_FUSE, plan->aux_stream));
+    } else {
+      for (int32_t st = CB_STAGE_DEVIATION; st <= CB_STAGE_FUSE; ++st)
+        CB_TRY(enqueue_stage(plan, l, io, cand, sh, st, plan->aux_stream));
+    }
     const cudaStream_t a = attn_stream[(l - 1) % kAttnStreams];
     CB_TRY(cuda_status(cudaEventRecord(plan->ev_ready, plan->aux_stream), "layer inputs ready"));
     CB_TRY(cuda_status(cudaStreamWaitEvent(a, plan->ev_ready, 0), "layer inputs ready"));

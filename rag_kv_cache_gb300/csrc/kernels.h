@@ -31,6 +31,24 @@ cudaError_t launch_rope_rows(void* out, const void* x, RowMap imap, RowMap omap,
 
 // Deviation per candidate in the canonical fp32 order: V only when k_new is null, else K+V
 // (the key part turned to p_old = token mod chunk_len with the table and RoPE style).
+// Several layers' selections over one candidate list (the re-selection reading of the gradual
+// filter: every layer >= 2 selects from S_1): one launch of deviations (a grid row per layer) and
+// one of top-k (a block per layer), up to kSelectBatchMax layers. k_new / k_old null: V deviation.
+constexpr int kSelectBatchMax = 16;
+struct SelectBatch {
+  int n;
+  const void* k_new[kSelectBatchMax];
+  const void* k_old[kSelectBatchMax];
+  const void* v_new[kSelectBatchMax];
+  const void* v_old[kSelectBatchMax];
+  float* dev[kSelectBatchMax];
+  int32_t* sel_tok[kSelectBatchMax];
+  int32_t* sel_row[kSelectBatchMax];
+};
+cudaError_t launch_select_batch(const SelectBatch& b, const int32_t* cand, int32_t m, int32_t k, int32_t n_rows,
+                                int32_t hkv, int32_t head_dim, int32_t chunk_len, int32_t style, RopeTable t,
+                                int32_t* err, cudaStream_t s);
+
 cudaError_t launch_kv_deviation(const void* k_new, const void* k_old, const void* v_new, const void* v_old,
                                 const int32_t* cand, int32_t m, int32_t n_rows, int32_t hkv, int32_t head_dim,
                                 int32_t chunk_len, int32_t style, RopeTable t, float* dev, int32_t* err,

@@ -210,17 +210,13 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(uint8_t* out, const uint
 //   table row of p_old (first pair member x' = fl(fl(x c) - fl(y s)), second member
 //   y' = fl(fl(x s) + fl(y c))); then the V part. Each lane adds all its key chunks before
 //   its V chunks. Products and sums are separately rounded (no fused multiply-add).
+// Candidate i's deviation (one warp): the body of kv_deviation_kernel and of its batched form.
 template <int CPL, int KS>
-__global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* k_new, const uint8_t* k_old,
-                                                           const uint8_t* v_new, const uint8_t* v_old,
-                                                           const int32_t* cand, int m, int n_rows, int elems,
-                                                           int head_dim, int chunk_len, RopeTable tab, float* dev,
-                                                           int32_t* err) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void deviation_row(const uint8_t* k_new, const uint8_t* k_old, const uint8_t* v_new,
+                                              const uint8_t* v_old, const int32_t* cand, int i, int n_rows,
+                                              int elems, int head_dim, int chunk_len, RopeTable tab, float* dev,
+                                              int32_t* err) {
   const int lane = threadIdx.x % kWarp;
-  const int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
-  if (i >= m) return;
   const int t = cand ? cand[i] : i;
   if (t < 0 || t >= n_rows) {
     if (lane == 0) {
@@ -327,6 +323,34 @@ __global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* k_new,
   if (lane == 0) dev[i] = acc;
 }
 
+template <int CPL, int KS>
+__global__ void __launch_bounds__(256) kv_deviation_kernel(const uint8_t* k_new, const uint8_t* k_old,
+                                                           const uint8_t* v_new, const uint8_t* v_old,
+                                                           const int32_t* cand, int m, int n_rows, int elems,
+                                                           int head_dim, int chunk_len, RopeTable tab, float* dev,
+                                                           int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  if (i >= m) return;
+  deviation_row<CPL, KS>(k_new, k_old, v_new, v_old, cand, i, n_rows, elems, head_dim, chunk_len, tab, dev, err);
+}
+
+// The deviations of several layers over one candidate list (blockIdx.y = layer of the batch).
+template <int CPL, int KS>
+__global__ void __launch_bounds__(256) kv_deviation_batch_kernel(const __grid_constant__ SelectBatch b,
+                                                                 const int32_t* cand, int m, int n_rows, int elems,
+                                                                 int head_dim, int chunk_len, RopeTable tab,
+                                                                 int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+  const int l = blockIdx.y;
+  if (i >= m || l >= b.n) return;
+  deviation_row<CPL, KS>((const uint8_t*)b.k_new[l], (const uint8_t*)b.k_old[l], (const uint8_t*)b.v_new[l],
+                         (const uint8_t*)b.v_old[l], cand, i, n_rows, elems, head_dim, chunk_len, tab, b.dev[l], err);
+}
+
 // ---------------------------------------------------------------------------
 // Top-k by MSB-first 8-bit radix select on order-preserving keys, then a
 // stable compaction. One block of 1024 threads.
@@ -337,12 +361,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 constexpr int kTopkThreads = 1024;
 
-__global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __restrict__ dev,
-                                                                  const int32_t* __restrict__ cand, int m,
-                                                                  int k, int32_t* sel_tok, int32_t* sel_row,
-                                                                  int32_t* err) {
-  pdl_launch_dependents();
-  pdl_wait();
+// The selection of one list by one block of kTopkThreads: the body of hkvd_topk_kernel and of its
+// batched form.
+__device__ __forceinline__ void topk_block(const float* __restrict__ dev, const int32_t* __restrict__ cand, int m,
+                                           int k, int32_t* sel_tok, int32_t* sel_row, int32_t* err) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_remaining;
@@ -458,6 +480,26 @@ __global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __
     }
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) hkvd_topk_kernel(const float* __restrict__ dev,
+                                                                  const int32_t* __restrict__ cand, int m,
+                                                                  int k, int32_t* sel_tok, int32_t* sel_row,
+                                                                  int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
+  topk_block(dev, cand, m, k, sel_tok, sel_row, err);
+}
+
+// The selections of several layers over one candidate list (block l = layer l of the batch).
+__global__ void __launch_bounds__(kTopkThreads) hkvd_topk_batch_kernel(const __grid_constant__ SelectBatch b,
+                                                                        const int32_t* __restrict__ cand, int m,
+                                                                        int k, int32_t* err) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int l = blockIdx.x;
+  if (l >= b.n) return;
+  topk_block(b.dev[l], cand, m, k, b.sel_tok[l], b.sel_row[l], err);
 }
 
 // ---------------------------------------------------------------------------
@@ -669,6 +711,39 @@ cudaError_t launch_kv_deviation(const void* k_new, const void* k_old, const void
                                     err, s);
   return launch_kv_deviation_t<1>(k_new, k_old, v_new, v_old, cand, m, n_rows, hkv, head_dim, chunk_len, t, dev, err,
                                   s);
+}
+
+template <int KS>
+static cudaError_t launch_select_batch_t(const SelectBatch& b, const int32_t* cand, int32_t m, int32_t k,
+                                         int32_t n_rows, int32_t hkv, int32_t head_dim, int32_t chunk_len,
+                                         RopeTable t, int32_t* err, cudaStream_t s) {
+  const int elems = hkv * head_dim;
+  const int cpl = (elems + 255) / 256;
+  const dim3 grid((m + 7) / 8, b.n);
+  cudaError_t e;
+#define CB_DEVB_LAUNCH(C) \
+  e = launch_pdl(kv_deviation_batch_kernel<C, KS>, grid, 256, 0, s, b, cand, m, n_rows, elems, head_dim, chunk_len, t, err)
+  if (cpl <= 1)
+    CB_DEVB_LAUNCH(1);
+  else if (cpl <= 2)
+    CB_DEVB_LAUNCH(2);
+  else if (cpl <= 4)
+    CB_DEVB_LAUNCH(4);
+  else
+    CB_DEVB_LAUNCH(8);
+#undef CB_DEVB_LAUNCH
+  if (e != cudaSuccess || k <= 0) return e;
+  return launch_pdl(hkvd_topk_batch_kernel, b.n, kTopkThreads, 0, s, b, cand, m, k, err);
+}
+
+cudaError_t launch_select_batch(const SelectBatch& b, const int32_t* cand, int32_t m, int32_t k, int32_t n_rows,
+                                int32_t hkv, int32_t head_dim, int32_t chunk_len, int32_t style, RopeTable t,
+                                int32_t* err, cudaStream_t s) {
+  if (m <= 0 || b.n <= 0) return cudaSuccess;
+  if (b.n > kSelectBatchMax) return cudaErrorInvalidValue;
+  if (b.k_new[0] == nullptr) return launch_select_batch_t<-1>(b, cand, m, k, n_rows, hkv, head_dim, 1, t, err, s);
+  if (style == 0) return launch_select_batch_t<0>(b, cand, m, k, n_rows, hkv, head_dim, chunk_len, t, err, s);
+  return launch_select_batch_t<1>(b, cand, m, k, n_rows, hkv, head_dim, chunk_len, t, err, s);
 }
 
 cudaError_t launch_hkvd_topk(const float* dev, const int32_t* cand, int32_t m, int32_t k, int32_t* sel_tok,

@@ -220,7 +220,9 @@ def test_full_size_kv_reselect(cb):
 
 
 @pytest.mark.parametrize("name,layers,deviation,filter", [("mistral7b", 4, "v", "keep"), ("tiny", 1, "v", "keep"),
-                                                          ("mistral7b", 4, "kv", "reselect")])
+                                                          ("mistral7b", 4, "kv", "reselect"),
+                                                          ("mistral7b", 20, "v", "reselect"),  # two selection batches
+                                                          ("mistral7b", 18, "kv", "reselect")])
 def test_request_scheduling_matches_layer_by_layer(cb, name, layers, deviation, filter):
     # cb_blend_request overlaps layers on several streams; its outputs must be the same bytes
     # as calling cb_blend_layer layer after layer.
