@@ -14,10 +14,12 @@
 // gathered rows, two 128-wide heads or four 64-wide heads of one of Q, K, V). Warp 0 feeds a
 // 4-stage ring with TMA: the 128 x 64 slice of the gathered rows and the 256 x 64 slice of W,
 // both 128-byte swizzled; warp 1 issues tcgen05.mma (M 128, N 256, K 16; bf16 in,
-// fp32 accumulate in 256 TMEM columns), one commit per stage frees its slot; warps 4-7 (TMEM lanes
-// 0-127, one output row per thread) turn the finished accumulator into bf16 rows. Every mbarrier
-// wait is bounded (2 s); a timeout records an error, the CTA drains its copies and MMAs, frees
-// TMEM and returns.
+// fp32 accumulate in 256 TMEM columns), one commit per stage frees its slot; both poll their
+// barriers (a sleeping wait resumes hundreds of cycles late, which the 4-stage ring cannot hide).
+// Warps 4-7 (TMEM lanes 0-127, one output row per thread) turn the finished accumulator into
+// bf16 rows in the drained ring: the tile's cos/sin rows come in coalesced (one token row per
+// warp instruction), the RoPE-encoded rows go out coalesced. Every mbarrier wait is bounded
+// (2 s); a timeout records an error, the CTA drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -60,8 +62,9 @@ struct ProjBars {
   uint64_t drain;
 };
 
-// Rows of X to a contiguous [m, d_model] buffer: one warp per row, 16-byte accesses; an index
-// outside X gives a zero row and an error record.
+// Rows of X to a contiguous [m, d_model] buffer: one warp per row, 16-byte accesses, up to 8 KiB
+// of a row's loads in flight before its stores; an index outside X gives a zero row and an error
+// record.
 __global__ void __launch_bounds__(256) gather_rows_kernel(uint8_t* dst, const uint8_t* src, const int32_t* rows,
                                                           int m, int n_src, int row_bytes, int32_t* err) {
   pdl_launch_dependents();
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(uint8_t* dst, const ui
     return;
   }
   const uint8_t* sp = src + (size_t)t * row_bytes;
-  constexpr int B = 4;
+  constexpr int B = 16;
   for (int c0 = lane * 16; c0 < row_bytes; c0 += 32 * 16 * B) {
     uint4 v[B];
 #pragma unroll
@@ -87,6 +90,26 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(uint8_t* dst, const ui
       if (c0 + b * 512 < row_bytes) st_stream(d + c0 + b * 512, v[b]);
   }
 }
+
+// Shared-memory accesses by 32-bit shared-window address, and the 16-byte global -> shared copy
+// (cp.async, cached in L2 only) with its wait.
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u4(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
   asm volatile(
@@ -152,7 +175,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int kk = 0; kk < n_k; ++kk) {
         const int st = kk % kPStages;
         if (kk >= kPStages &&
-            !mbar_wait(smem_u32(&bars.empty[st]), ((kk / kPStages) - 1) & 1, abort_flag, p.err, 40))
+            !mbar_spin(smem_u32(&bars.empty[st]), ((kk / kPStages) - 1) & 1, abort_flag, p.err, 40))
           break;
         const uint32_t fb = smem_u32(&bars.full[st]);
         mbar_expect_tx(fb, kPABytes + kPBBytes);
@@ -172,7 +195,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     for (int kk = 0; kk < n_k && ok; ++kk) {
       const int st = kk % kPStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.full[st]), (kk / kPStages) & 1, abort_flag, p.err, 42));
+      ok = __all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.full[st]), (kk / kPStages) & 1, abort_flag, p.err, 42));
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
@@ -192,53 +215,66 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncwarp();
     mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 43, false);
   } else if (warp >= 4) {
-    const int r = (warp - 4) * 32 + lane;  // TMEM lane = output row of the tile
-    const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const int ew = warp - 4;  // TMEM lanes and tile rows 32 ew .. 32 ew + 31
+    const int r = ew * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(ew * 32) << 16);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.acc_full), 0, abort_flag, p.err, 44));
     if (ok) {
       tc_fence_after();
-      const int t = s_rows[r];
-      const bool store = m0 + r < p.m && t >= 0;
+      // Every MMA has completed, so the ring is free: it stages the tile's cos/sin rows (loaded
+      // coalesced, one token row per warp instruction) and the bf16 output rows (stored
+      // coalesced, one tile row per warp instruction). Row pitches are 16 bytes past a multiple
+      // of 128, so a thread per row touches every bank once per 16-byte step.
+      constexpr uint32_t kOutPitch = kPN * 2 + 16;
+      constexpr uint32_t kTabPitch = D * 4 + 16;  // D / 2 (cos, sin) pairs
+      const uint32_t out_s = sA0;
+      const uint32_t tab_s = sA0 + kPM * kOutPitch;
+      const int n_qk = (p.hq + p.hkv) * D;  // features that RoPE encodes
+      const bool rope_tile = p.encode != 0 && n0 < n_qk;
+      if (rope_tile) {
+        for (int i = 0; i < 32; ++i) {
+          const int t = s_rows[ew * 32 + i];
+          if (t >= 0 && lane * 16 < D * 4)
+            cp_async16(tab_s + (uint32_t)(ew * 32 + i) * kTabPitch + lane * 16,
+                       reinterpret_cast<const uint8_t*>(p.tab + (size_t)t * (D / 2)) + lane * 16);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+      }
+      const uint32_t my_out = out_s + (uint32_t)r * kOutPitch;
+      const uint32_t my_tab = tab_s + (uint32_t)r * kTabPitch;
       constexpr int kHeads = kPN / D;
 #pragma unroll 1
       for (int hh = 0; hh < kHeads; ++hh) {
         const int f0 = n0 + hh * D;  // first output feature of this head
-        if (f0 >= (p.hq + 2 * p.hkv) * D) break;  // the last tile may reach past W (read as zeros)
-        uint8_t* dst;
-        bool rope;
-        if (f0 < p.hq * D) {
-          dst = p.q + ((size_t)t * p.hq + f0 / D) * D * 2;
-          rope = p.encode != 0;
-        } else if (f0 < (p.hq + p.hkv) * D) {
-          dst = p.k + ((size_t)t * p.hkv + (f0 / D - p.hq)) * D * 2;
-          rope = p.encode != 0;
-        } else {
-          dst = p.v + ((size_t)t * p.hkv + (f0 / D - p.hq - p.hkv)) * D * 2;
-          rope = false;
-        }
+        // warp-uniform (tcgen05.ld is a whole-warp instruction): a row without a token computes
+        // from unloaded table entries and is never stored
+        const bool rope = rope_tile && f0 < n_qk;
         const uint32_t col = lane_base + hh * D;
         if (rope && p.style == 0) {
           // pairs (j, j + D/2): columns j0.. and D/2 + j0.. of the head
-          const float2* cs = p.tab + (size_t)(t < 0 ? 0 : t) * (D / 2);
 #pragma unroll 1
           for (int j0 = 0; j0 < D / 2; j0 += 32) {
             uint32_t a[32], b[32];
-            tmem_ld_x32(col + j0, a);
-            tmem_ld_x32(col + D / 2 + j0, b);
-            if (store) {
-              float oa[32], ob[32];
+            tmem_ld_x32_async(col + j0, a);
+            tmem_ld_x32_async(col + D / 2 + j0, b);
+            tmem_wait_ld(a);
+            tmem_wait_ld(b);
+            float oa[32], ob[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float2 c = cs[j0 + e];
-                const float x = __uint_as_float(a[e]), y = __uint_as_float(b[e]);
-                oa[e] = x * c.x - y * c.y;
-                ob[e] = x * c.y + y * c.x;
-              }
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const float4 c = lds_f4(my_tab + (uint32_t)(j0 + 2 * e2) * 8);  // pairs j0 + 2 e2, + 1
+              const float x0 = __uint_as_float(a[2 * e2]), y0 = __uint_as_float(b[2 * e2]);
+              const float x1 = __uint_as_float(a[2 * e2 + 1]), y1 = __uint_as_float(b[2 * e2 + 1]);
+              oa[2 * e2] = x0 * c.x - y0 * c.y;
+              ob[2 * e2] = x0 * c.y + y0 * c.x;
+              oa[2 * e2 + 1] = x1 * c.z - y1 * c.w;
+              ob[2 * e2 + 1] = x1 * c.w + y1 * c.z;
+            }
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                *reinterpret_cast<uint4*>(dst + (j0 + q4 * 8) * 2) = pack8(oa + q4 * 8);
-                *reinterpret_cast<uint4*>(dst + (D / 2 + j0 + q4 * 8) * 2) = pack8(ob + q4 * 8);
-              }
+            for (int q4 = 0; q4 < 4; ++q4) {
+              sts_u4(my_out + (uint32_t)(hh * D + j0 + q4 * 8) * 2, pack8(oa + q4 * 8));
+              sts_u4(my_out + (uint32_t)(hh * D + D / 2 + j0 + q4 * 8) * 2, pack8(ob + q4 * 8));
             }
           }
         } else {
@@ -246,24 +282,46 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t a[32];
             tmem_ld_x32(col + c0, a);
-            if (store) {
-              float o[32];
+            float o[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
-              if (rope) {  // pairs (2j, 2j + 1)
-                const float2* cs = p.tab + (size_t)t * (D / 2) + c0 / 2;
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
+            if (rope) {  // pairs (2j, 2j + 1)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const float2 c = cs[e];
-                  const float x = o[2 * e], y = o[2 * e + 1];
-                  o[2 * e] = x * c.x - y * c.y;
-                  o[2 * e + 1] = x * c.y + y * c.x;
-                }
+              for (int e2 = 0; e2 < 8; ++e2) {
+                const float4 c = lds_f4(my_tab + (uint32_t)(c0 / 2 + 2 * e2) * 8);
+                const float x0 = o[4 * e2], y0 = o[4 * e2 + 1], x1 = o[4 * e2 + 2], y1 = o[4 * e2 + 3];
+                o[4 * e2] = x0 * c.x - y0 * c.y;
+                o[4 * e2 + 1] = x0 * c.y + y0 * c.x;
+                o[4 * e2 + 2] = x1 * c.z - y1 * c.w;
+                o[4 * e2 + 3] = x1 * c.w + y1 * c.z;
               }
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) *reinterpret_cast<uint4*>(dst + (c0 + q4 * 8) * 2) = pack8(o + q4 * 8);
             }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) sts_u4(my_out + (uint32_t)(hh * D + c0 + q4 * 8) * 2, pack8(o + q4 * 8));
           }
+        }
+      }
+      __syncwarp();
+      // Coalesced stores of this warp's 32 rows: lane l takes tile features 8 l .. 8 l + 7.
+      const int f = n0 + lane * 8;
+      const int n_out = (p.hq + 2 * p.hkv) * D;
+      uint8_t* dst_base = nullptr;
+      int heads_in = 0, head = 0;
+      if (f < p.hq * D) {
+        dst_base = p.q; heads_in = p.hq; head = f / D;
+      } else if (f < n_qk) {
+        dst_base = p.k; heads_in = p.hkv; head = f / D - p.hq;
+      } else if (f < n_out) {
+        dst_base = p.v; heads_in = p.hkv; head = f / D - p.hq - p.hkv;
+      }
+      const size_t col_bytes = (size_t)head * D * 2 + (size_t)(f % D) * 2;
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {
+        const int row = ew * 32 + i;
+        const int ti = s_rows[row];
+        if (m0 + row < p.m && ti >= 0 && dst_base != nullptr) {
+          const uint4 val = lds_u4(out_s + (uint32_t)row * kOutPitch + lane * 16);
+          *reinterpret_cast<uint4*>(dst_base + (size_t)ti * heads_in * D * 2 + col_bytes) = val;
         }
       }
     }

@@ -92,3 +92,33 @@ def test_bad_row_is_recorded_and_skipped(cb):
     with pytest.raises(cb.CacheBlendError):  # d_model not a multiple of 64
         cb.cb_qkv_projection(plan, bf16_tensor(x[:, :100].copy()), None, 4, bf16_tensor(w[:, :100].copy()), q, k, v)
     plan.close()
+
+
+def test_gathered_rows_repeat_bit_identical(cb):
+    # Back-to-back launches share the gather workspace and the tiles' shared-memory staging (the
+    # epilogue reuses the TMA ring); a read of stale rows or staging would show as launches
+    # that differ. Two inputs alternate over 16 launches at the Mistral-7B shape (524 rows =
+    # 4 full tiles and a 12-row tail): every launch equals the first one on its input bit for bit.
+    cfg = get_config("mistral7b")
+    plan = cb.Plan.from_config(cfg)
+    rng = np.random.default_rng(524)
+    rows = _i32(np.concatenate([np.sort(rng.choice(cfg.n_ctx, 460, replace=False)),
+                                np.arange(cfg.n_ctx, cfg.n_tokens)]))
+    inputs = [tuple(bf16_tensor(a) for a in generate_projection(cfg, s)) for s in (1, 2)]
+    shape = lambda h: (cfg.n_tokens, h, cfg.head_dim)
+    xg = torch.empty((524, cfg.d_model), dtype=torch.bfloat16, device="cuda")
+    first = [None, None]
+    for it in range(16):
+        x, w = inputs[it % 2]
+        q = torch.zeros(shape(cfg.hq), dtype=torch.bfloat16, device="cuda")
+        k = torch.zeros(shape(cfg.hkv), dtype=torch.bfloat16, device="cuda")
+        v = torch.zeros(shape(cfg.hkv), dtype=torch.bfloat16, device="cuda")
+        cb.cb_qkv_projection(plan, x, rows, 524, w, q, k, v, encode=True, x_gathered=xg)
+        got = torch.cat([q.flatten(), k.flatten(), v.flatten()])
+        if first[it % 2] is None:
+            first[it % 2] = got
+        else:
+            assert torch.equal(got.view(torch.int16), first[it % 2].view(torch.int16)), f"launch {it}"
+    plan.check()
+    assert not torch.equal(first[0], first[1])
+    plan.close()
