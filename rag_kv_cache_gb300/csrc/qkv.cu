@@ -16,9 +16,10 @@
 // both 128-byte swizzled; warp 1 issues tcgen05.mma (M 128, N 256, K 16; bf16 in,
 // fp32 accumulate in 256 TMEM columns), one commit per stage frees its slot; both poll their
 // barriers (a sleeping wait resumes hundreds of cycles late, which the 4-stage ring cannot hide).
-// Warps 4-7 (TMEM lanes 0-127, one output row per thread) turn the finished accumulator into
-// bf16 rows in the drained ring: the tile's cos/sin rows come in coalesced (one token row per
-// warp instruction), the RoPE-encoded rows go out coalesced. Every mbarrier wait is bounded
+// Then all eight warps turn the finished accumulator into bf16 rows in the drained ring (one
+// output row per thread; warps g and g + 4 read TMEM lanes 32 g .. 32 g + 31 and take half of the
+// tile's heads each): the tile's cos/sin rows come in coalesced (one token row per warp
+// instruction), the RoPE-encoded rows go out coalesced. Every mbarrier wait is bounded
 // (2 s); a timeout records an error, the CTA drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -110,6 +111,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Named barrier of the two warps g and g + 4 of the epilogue (ids 1-4; 0 is __syncthreads).
+__device__ __forceinline__ void pair_bar_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
   asm volatile(
@@ -214,115 +217,120 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (elect_one()) tc_commit(smem_u32(&bars.drain));
     __syncwarp();
     mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 43, false);
-  } else if (warp >= 4) {
-    const int ew = warp - 4;  // TMEM lanes and tile rows 32 ew .. 32 ew + 31
-    const int r = ew * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(ew * 32) << 16);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.acc_full), 0, abort_flag, p.err, 44));
-    if (ok) {
-      tc_fence_after();
-      // Every MMA has completed, so the ring is free: it stages the tile's cos/sin rows (loaded
-      // coalesced, one token row per warp instruction) and the bf16 output rows (stored
-      // coalesced, one tile row per warp instruction). Row pitches are 16 bytes past a multiple
-      // of 128, so a thread per row touches every bank once per 16-byte step.
-      constexpr uint32_t kOutPitch = kPN * 2 + 16;
-      constexpr uint32_t kTabPitch = D * 4 + 16;  // D / 2 (cos, sin) pairs
-      const uint32_t out_s = sA0;
-      const uint32_t tab_s = sA0 + kPM * kOutPitch;
-      const int n_qk = (p.hq + p.hkv) * D;  // features that RoPE encodes
-      const bool rope_tile = p.encode != 0 && n0 < n_qk;
-      if (rope_tile) {
-        for (int i = 0; i < 32; ++i) {
-          const int t = s_rows[ew * 32 + i];
-          if (t >= 0 && lane * 16 < D * 4)
-            cp_async16(tab_s + (uint32_t)(ew * 32 + i) * kTabPitch + lane * 16,
-                       reinterpret_cast<const uint8_t*>(p.tab + (size_t)t * (D / 2)) + lane * 16);
-        }
-        cp_async_wait_all();
-        __syncwarp();
+  }
+
+  // Epilogue on all eight warps: warps g and g + 4 share TMEM lanes 32 g .. 32 g + 31 (the tile
+  // rows of group g) and split the tile's heads; a named barrier per pair orders their shared
+  // staging. Whether the accumulator is complete is decided for the whole CTA, so a wait that
+  // gave up in one warp cannot leave its partner at a pair barrier.
+  const bool acc_ok = mbar_wait(smem_u32(&bars.acc_full), 0, abort_flag, p.err, 44);
+  if (__syncthreads_and(acc_ok ? 1 : 0)) {
+    tc_fence_after();
+    const int g = warp & 3, upper = warp >> 2;
+    const int r = g * 32 + lane;
+    const int half_rows = g * 32 + (upper ? 0 : 16);  // the 16 rows this warp loads and stores
+    const uint32_t lane_base = tmem + ((uint32_t)(g * 32) << 16);
+    // Every MMA has completed, so the ring is free: it stages the tile's cos/sin rows (loaded
+    // coalesced, one token row per warp instruction) and the bf16 output rows (stored
+    // coalesced, one tile row per warp instruction). Row pitches are 16 bytes past a multiple
+    // of 128, so a thread per row touches every bank once per 16-byte step.
+    constexpr uint32_t kOutPitch = kPN * 2 + 16;
+    constexpr uint32_t kTabPitch = D * 4 + 16;  // D / 2 (cos, sin) pairs
+    const uint32_t out_s = sA0;
+    const uint32_t tab_s = sA0 + kPM * kOutPitch;
+    const int n_qk = (p.hq + p.hkv) * D;  // features that RoPE encodes
+    const bool rope_tile = p.encode != 0 && n0 < n_qk;
+    if (rope_tile) {
+      for (int i = 0; i < 16; ++i) {
+        const int t = s_rows[half_rows + i];
+        if (t >= 0 && lane * 16 < D * 4)
+          cp_async16(tab_s + (uint32_t)(half_rows + i) * kTabPitch + lane * 16,
+                     reinterpret_cast<const uint8_t*>(p.tab + (size_t)t * (D / 2)) + lane * 16);
       }
-      const uint32_t my_out = out_s + (uint32_t)r * kOutPitch;
-      const uint32_t my_tab = tab_s + (uint32_t)r * kTabPitch;
-      constexpr int kHeads = kPN / D;
+      cp_async_wait_all();
+    }
+    pair_bar_sync(1 + g);
+    const uint32_t my_out = out_s + (uint32_t)r * kOutPitch;
+    const uint32_t my_tab = tab_s + (uint32_t)r * kTabPitch;
+    constexpr int kHeads = kPN / D;
 #pragma unroll 1
-      for (int hh = 0; hh < kHeads; ++hh) {
-        const int f0 = n0 + hh * D;  // first output feature of this head
-        // warp-uniform (tcgen05.ld is a whole-warp instruction): a row without a token computes
-        // from unloaded table entries and is never stored
-        const bool rope = rope_tile && f0 < n_qk;
-        const uint32_t col = lane_base + hh * D;
-        if (rope && p.style == 0) {
-          // pairs (j, j + D/2): columns j0.. and D/2 + j0.. of the head
+    for (int hh = upper ? 0 : kHeads / 2; hh < (upper ? kHeads / 2 : kHeads); ++hh) {
+      const int f0 = n0 + hh * D;  // first output feature of this head
+      // warp-uniform (tcgen05.ld is a whole-warp instruction): a row without a token computes
+      // from unloaded table entries and is never stored
+      const bool rope = rope_tile && f0 < n_qk;
+      const uint32_t col = lane_base + hh * D;
+      if (rope && p.style == 0) {
+        // pairs (j, j + D/2): columns j0.. and D/2 + j0.. of the head
 #pragma unroll 1
-          for (int j0 = 0; j0 < D / 2; j0 += 32) {
-            uint32_t a[32], b[32];
-            tmem_ld_x32_async(col + j0, a);
-            tmem_ld_x32_async(col + D / 2 + j0, b);
-            tmem_wait_ld(a);
-            tmem_wait_ld(b);
-            float oa[32], ob[32];
+        for (int j0 = 0; j0 < D / 2; j0 += 32) {
+          uint32_t a[32], b[32];
+          tmem_ld_x32_async(col + j0, a);
+          tmem_ld_x32_async(col + D / 2 + j0, b);
+          tmem_wait_ld(a);
+          tmem_wait_ld(b);
+          float oa[32], ob[32];
 #pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-              const float4 c = lds_f4(my_tab + (uint32_t)(j0 + 2 * e2) * 8);  // pairs j0 + 2 e2, + 1
-              const float x0 = __uint_as_float(a[2 * e2]), y0 = __uint_as_float(b[2 * e2]);
-              const float x1 = __uint_as_float(a[2 * e2 + 1]), y1 = __uint_as_float(b[2 * e2 + 1]);
-              oa[2 * e2] = x0 * c.x - y0 * c.y;
-              ob[2 * e2] = x0 * c.y + y0 * c.x;
-              oa[2 * e2 + 1] = x1 * c.z - y1 * c.w;
-              ob[2 * e2 + 1] = x1 * c.w + y1 * c.z;
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              sts_u4(my_out + (uint32_t)(hh * D + j0 + q4 * 8) * 2, pack8(oa + q4 * 8));
-              sts_u4(my_out + (uint32_t)(hh * D + D / 2 + j0 + q4 * 8) * 2, pack8(ob + q4 * 8));
-            }
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const float4 c = lds_f4(my_tab + (uint32_t)(j0 + 2 * e2) * 8);  // pairs j0 + 2 e2, + 1
+            const float x0 = __uint_as_float(a[2 * e2]), y0 = __uint_as_float(b[2 * e2]);
+            const float x1 = __uint_as_float(a[2 * e2 + 1]), y1 = __uint_as_float(b[2 * e2 + 1]);
+            oa[2 * e2] = x0 * c.x - y0 * c.y;
+            ob[2 * e2] = x0 * c.y + y0 * c.x;
+            oa[2 * e2 + 1] = x1 * c.z - y1 * c.w;
+            ob[2 * e2 + 1] = x1 * c.w + y1 * c.z;
           }
-        } else {
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t a[32];
-            tmem_ld_x32(col + c0, a);
-            float o[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
-            if (rope) {  // pairs (2j, 2j + 1)
-#pragma unroll
-              for (int e2 = 0; e2 < 8; ++e2) {
-                const float4 c = lds_f4(my_tab + (uint32_t)(c0 / 2 + 2 * e2) * 8);
-                const float x0 = o[4 * e2], y0 = o[4 * e2 + 1], x1 = o[4 * e2 + 2], y1 = o[4 * e2 + 3];
-                o[4 * e2] = x0 * c.x - y0 * c.y;
-                o[4 * e2 + 1] = x0 * c.y + y0 * c.x;
-                o[4 * e2 + 2] = x1 * c.z - y1 * c.w;
-                o[4 * e2 + 3] = x1 * c.w + y1 * c.z;
-              }
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) sts_u4(my_out + (uint32_t)(hh * D + c0 + q4 * 8) * 2, pack8(o + q4 * 8));
+          for (int q4 = 0; q4 < 4; ++q4) {
+            sts_u4(my_out + (uint32_t)(hh * D + j0 + q4 * 8) * 2, pack8(oa + q4 * 8));
+            sts_u4(my_out + (uint32_t)(hh * D + D / 2 + j0 + q4 * 8) * 2, pack8(ob + q4 * 8));
           }
         }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld_x32(col + c0, a);
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(a[e]);
+          if (rope) {  // pairs (2j, 2j + 1)
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) {
+              const float4 c = lds_f4(my_tab + (uint32_t)(c0 / 2 + 2 * e2) * 8);
+              const float x0 = o[4 * e2], y0 = o[4 * e2 + 1], x1 = o[4 * e2 + 2], y1 = o[4 * e2 + 3];
+              o[4 * e2] = x0 * c.x - y0 * c.y;
+              o[4 * e2 + 1] = x0 * c.y + y0 * c.x;
+              o[4 * e2 + 2] = x1 * c.z - y1 * c.w;
+              o[4 * e2 + 3] = x1 * c.w + y1 * c.z;
+            }
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) sts_u4(my_out + (uint32_t)(hh * D + c0 + q4 * 8) * 2, pack8(o + q4 * 8));
+        }
       }
-      __syncwarp();
-      // Coalesced stores of this warp's 32 rows: lane l takes tile features 8 l .. 8 l + 7.
-      const int f = n0 + lane * 8;
-      const int n_out = (p.hq + 2 * p.hkv) * D;
-      uint8_t* dst_base = nullptr;
-      int heads_in = 0, head = 0;
-      if (f < p.hq * D) {
-        dst_base = p.q; heads_in = p.hq; head = f / D;
-      } else if (f < n_qk) {
-        dst_base = p.k; heads_in = p.hkv; head = f / D - p.hq;
-      } else if (f < n_out) {
-        dst_base = p.v; heads_in = p.hkv; head = f / D - p.hq - p.hkv;
-      }
-      const size_t col_bytes = (size_t)head * D * 2 + (size_t)(f % D) * 2;
+    }
+    pair_bar_sync(1 + g);
+    // Coalesced stores of this warp's 16 rows: lane l takes tile features 8 l .. 8 l + 7.
+    const int f = n0 + lane * 8;
+    const int n_out = (p.hq + 2 * p.hkv) * D;
+    uint8_t* dst_base = nullptr;
+    int heads_in = 0, head = 0;
+    if (f < p.hq * D) {
+      dst_base = p.q; heads_in = p.hq; head = f / D;
+    } else if (f < n_qk) {
+      dst_base = p.k; heads_in = p.hkv; head = f / D - p.hq;
+    } else if (f < n_out) {
+      dst_base = p.v; heads_in = p.hkv; head = f / D - p.hq - p.hkv;
+    }
+    const size_t col_bytes = (size_t)head * D * 2 + (size_t)(f % D) * 2;
 #pragma unroll 4
-      for (int i = 0; i < 32; ++i) {
-        const int row = ew * 32 + i;
-        const int ti = s_rows[row];
-        if (m0 + row < p.m && ti >= 0 && dst_base != nullptr) {
-          const uint4 val = lds_u4(out_s + (uint32_t)row * kOutPitch + lane * 16);
-          *reinterpret_cast<uint4*>(dst_base + (size_t)ti * heads_in * D * 2 + col_bytes) = val;
-        }
+    for (int i = 0; i < 16; ++i) {
+      const int row = half_rows + i;
+      const int ti = s_rows[row];
+      if (m0 + row < p.m && ti >= 0 && dst_base != nullptr) {
+        const uint4 val = lds_u4(out_s + (uint32_t)row * kOutPitch + lane * 16);
+        *reinterpret_cast<uint4*>(dst_base + (size_t)ti * heads_in * D * 2 + col_bytes) = val;
       }
     }
   }
