@@ -10,17 +10,25 @@
 //
 // The candidate rows of X are first gathered into a contiguous workspace by a streaming kernel
 // (2 m d_model bytes each way): a 128-byte-swizzled TMA tile must land on a 1024-byte boundary,
-// which four-row gathers into one tile cannot all meet. One CTA per 128 x 256 output tile (128
-// gathered rows, two 128-wide heads or four 64-wide heads of one of Q, K, V). Warp 0 feeds a
-// 4-stage ring with TMA: the 128 x 64 slice of the gathered rows and the 256 x 64 slice of W,
-// both 128-byte swizzled; warp 1 issues tcgen05.mma (M 128, N 256, K 16; bf16 in,
-// fp32 accumulate in 256 TMEM columns), one commit per stage frees its slot; both poll their
-// barriers (a sleeping wait resumes hundreds of cycles late, which the 4-stage ring cannot hide).
-// Then all eight warps turn the finished accumulator into bf16 rows in the drained ring (one
-// output row per thread; warps g and g + 4 read TMEM lanes 32 g .. 32 g + 31 and take half of the
-// tile's heads each): the tile's cos/sin rows come in coalesced (one token row per warp
-// instruction), the RoPE-encoded rows go out coalesced. Every mbarrier wait is bounded
-// (2 s); a timeout records an error, the CTA drains its copies and MMAs, frees TMEM and returns.
+// which four-row gathers into one tile cannot all meet. A cluster of two CTAs then computes a
+// 256 x 256 output tile with tcgen05 cta_group::2: CTA r holds 128 gathered rows and W rows
+// n0 + 128 r .. n0 + 128 r + 127 of the tile's 256 output features (two 128-wide heads or four
+// 64-wide heads of one of Q, K, V), and the pair's MMA (M 256, N 256, K 16; bf16 in, fp32
+// accumulate), issued by CTA 0, reads both CTAs' shared memory and leaves each CTA's 128 rows x
+// 256 features in 256 columns of its own TMEM. Holding half of each W slice per SM makes a
+// stage 32 KiB (128 x 64 of X and of W, 128-byte swizzled), so seven stages fit and cover the
+// load latency, which four 48 KiB stages of a one-CTA 128 x 256 tile could not (its tensor pipe
+// idled a quarter of the K loop). Warp 0 of each CTA issues its loads, which complete on CTA 0's
+// "full" barrier (the cta_group::2 form of the tensor copy; CTA 0 expects the pair's bytes);
+// warp 1 of CTA 0 issues the MMAs and commits each stage to both CTAs' "empty" barriers
+// (multicast); both poll their barriers (a sleeping wait resumes hundreds of cycles late).
+// TMEM allocation, barrier set-up and the first W slices' L2 prefetch happen before the wait
+// on the kernels this one depends on. Then all eight warps of each CTA turn its accumulator
+// into bf16 rows in the drained ring (one output row per thread; warps g and g + 4 read TMEM
+// lanes 32 g .. 32 g + 31 and take half of the tile's heads each): the tile's cos/sin rows come
+// in coalesced (one token row per warp instruction), the RoPE-encoded rows go out coalesced.
+// Every mbarrier wait is bounded (2 s); a timeout records an error, the CTA drains its copies
+// and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,9 +43,6 @@ namespace {
 constexpr int kPM = 128;  // gathered rows per tile
 constexpr int kPN = 256;  // output features per tile
 constexpr int kPK = 64;   // K slice per stage (one 128-byte swizzle row of bf16)
-constexpr int kPStages = 4;
-constexpr uint32_t kPABytes = kPM * kPK * 2;  // 16 KiB
-constexpr uint32_t kPBBytes = kPN * kPK * 2;  // 32 KiB
 constexpr int kPThreads = 256;
 constexpr uint32_t kPTmemCols = 256;
 
@@ -54,13 +59,6 @@ struct ProjParams {
   uint8_t* k;
   uint8_t* v;
   int32_t* err;
-};
-
-struct ProjBars {
-  uint64_t full[kPStages];
-  uint64_t empty[kPStages];
-  uint64_t acc_full;
-  uint64_t drain;
 };
 
 // Rows of X to a contiguous [m, d_model] buffer: one warp per row, 16-byte accesses, up to 8 KiB
@@ -114,116 +112,15 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Named barrier of the two warps g and g + 4 of the epilogue (ids 1-4; 0 is __syncthreads).
 __device__ __forceinline__ void pair_bar_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
+// Epilogue on all eight warps: warps g and g + 4 share TMEM lanes 32 g .. 32 g + 31 (the tile
+// rows of group g) and split the tile's heads; a named barrier per pair orders their shared
+// staging. Whether the accumulator is complete is decided for the whole CTA, so a wait that
+// gave up in one warp cannot leave its partner at a pair barrier.
 template <int D>
-__global__ void __launch_bounds__(kPThreads, 1)
-    qkv_projection_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                          const ProjParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ ProjBars bars;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
-  __shared__ int s_rows[kPM];
-
-  pdl_launch_dependents();
-  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sA0 = base;
-  const uint32_t sB0 = base + kPStages * kPABytes;
+__device__ __forceinline__ void proj_epilogue(const ProjParams& p, uint32_t acc_bar, uint32_t tmem, uint32_t sA0,
+                                              const int* s_rows, int m0, int n0, volatile int* abort_flag) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int m0 = blockIdx.x * kPM;
-  const int n0 = blockIdx.y * kPN;
-  const int n_k = p.d_model / kPK;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(smem_u32(&bars.full[s]), 1);
-      mbar_init(smem_u32(&bars.empty[s]), 1);
-    }
-    mbar_init(smem_u32(&bars.acc_full), 1);
-    mbar_init(smem_u32(&bars.drain), 1);
-    s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(kPTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  pdl_wait();  // the rows and hidden states come from the kernels before this one
-  // Token id of each of the tile's rows (-1: past m, or an index the gather rejected: not stored).
-  if (threadIdx.x < kPM) {
-    const int i = m0 + (int)threadIdx.x;
-    int t = i < p.m ? (p.rows ? p.rows[i] : i) : -1;
-    if (t >= p.n_tokens) t = -1;
-    s_rows[threadIdx.x] = t;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  volatile int* abort_flag = &s_abort;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int kk = 0; kk < n_k; ++kk) {
-        const int st = kk % kPStages;
-        if (kk >= kPStages &&
-            !mbar_spin(smem_u32(&bars.empty[st]), ((kk / kPStages) - 1) & 1, abort_flag, p.err, 40))
-          break;
-        const uint32_t fb = smem_u32(&bars.full[st]);
-        mbar_expect_tx(fb, kPABytes + kPBBytes);
-        tma_load_2d(sA0 + st * kPABytes, &tm_x, fb, kk * kPK, m0);  // rows past m read as zeros
-        tma_load_2d(sB0 + st * kPBBytes, &tm_w, fb, kk * kPK, n0);
-        issued = kk + 1;
-      }
-      // every copy issued has landed before the CTA may exit
-      for (int kk = issued - kPStages < 0 ? 0 : issued - kPStages; kk < issued; ++kk)
-        mbar_wait(smem_u32(&bars.full[kk % kPStages]), (kk / kPStages) & 1, abort_flag, p.err, 41, false);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    constexpr uint32_t idesc = idesc_bf16(kPM, kPN, false);
-    const uint64_t da0 = sdesc(sA0, 16, 1024);
-    const uint64_t db0 = sdesc(sB0, 16, 1024);
-    bool ok = true;
-    for (int kk = 0; kk < n_k && ok; ++kk) {
-      const int st = kk % kPStages;
-      ok = __all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.full[st]), (kk / kPStages) & 1, abort_flag, p.err, 42));
-      if (!ok) break;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t da = da0 + (uint64_t)((st * kPABytes) >> 4);
-        const uint64_t db = db0 + (uint64_t)((st * kPBBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < kPK / 16; ++ks)
-          mma_ss(tmem, da + (uint64_t)((ks * 32) >> 4), db + (uint64_t)((ks * 32) >> 4), idesc,
-                 (kk > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&bars.empty[st]));
-        if (kk == n_k - 1) tc_commit(smem_u32(&bars.acc_full));
-      }
-      __syncwarp();
-    }
-    // all MMAs issued here complete before TMEM is freed
-    if (elect_one()) tc_commit(smem_u32(&bars.drain));
-    __syncwarp();
-    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 43, false);
-  }
-
-  // Epilogue on all eight warps: warps g and g + 4 share TMEM lanes 32 g .. 32 g + 31 (the tile
-  // rows of group g) and split the tile's heads; a named barrier per pair orders their shared
-  // staging. Whether the accumulator is complete is decided for the whole CTA, so a wait that
-  // gave up in one warp cannot leave its partner at a pair barrier.
-  const bool acc_ok = mbar_wait(smem_u32(&bars.acc_full), 0, abort_flag, p.err, 44);
+  const bool acc_ok = mbar_wait(acc_bar, 0, abort_flag, p.err, 44);
   if (__syncthreads_and(acc_ok ? 1 : 0)) {
     tc_fence_after();
     const int g = warp & 3, upper = warp >> 2;
@@ -334,12 +231,180 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   }
+}
+
+// ---- CTA-pair kernel ----
+constexpr int kQStages = 7;
+constexpr uint32_t kQHalfBytes = kPM * kPK * 2;  // 16 KiB: 128 rows x 64 of A, or of half of B
+
+struct PairBars {
+  uint64_t full[kQStages];   // CTA 0: both CTAs' A rows and W halves of the stage landed
+  uint64_t empty[kQStages];  // the pair's MMAs of the stage completed
+  uint64_t acc_full;             // every MMA completed
+  uint64_t drain;                // CTA 0's MMA issue loop ended and its MMAs completed
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_smem(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Tensor copy into this CTA's shared memory whose completion is counted on `bar_cluster`, a
+// barrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair once every MMA this
+// thread issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 1)
+    qkv_projection_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                               const ProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PairBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_rows[kPM];
+
+  pdl_launch_dependents();
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + kQStages * kQHalfBytes;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int m0 = blockIdx.x * kPM;          // this CTA's rows
+  const int n0 = blockIdx.y * kPN;          // the pair's 256 output features
+  const int nb = n0 + (int)rank * (kPN / 2);  // this CTA's half of the W slice
+  const int n_k = p.d_model / kPK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);  // used in CTA 0: its producer's expect_tx
+      mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.acc_full), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {  // one warp of each CTA allocates the pair's columns together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kPTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else if (threadIdx.x == 32) {
+    // While the kernels before this one finish: the tensor maps, and this CTA's first W slices
+    // into L2 (a prefetch only fills L2, so it cannot make a later load read stale data).
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_w) : "memory");
+    for (int kk = 0; kk < kQStages && kk < n_k; ++kk)
+      asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(&tm_w), "r"(kk * kPK), "r"(nb)
+                   : "memory");
+  }
+  // both CTAs' barriers initialised and TMEM allocated before any commit or MMA of the pair
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  pdl_wait();  // the rows and hidden states come from the kernels before this one
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t full0 = peer_smem(smem_u32(&bars.full[0]), 0);  // CTA 0's barriers
+      int issued = 0;
+      for (int kk = 0; kk < n_k; ++kk) {
+        const int st = kk % kQStages;
+        if (kk >= kQStages &&
+            !mbar_spin(smem_u32(&bars.empty[st]), ((kk / kQStages) - 1) & 1, abort_flag, p.err, 50))
+          break;
+        if (rank == 0) mbar_expect_tx(smem_u32(&bars.full[st]), 4 * kQHalfBytes);  // both CTAs' bytes
+        const uint32_t fb = full0 + (uint32_t)st * 8u;
+        tma_load_2d_pair(sA0 + st * kQHalfBytes, &tm_x, fb, kk * kPK, m0);  // rows past m read as zeros
+        tma_load_2d_pair(sB0 + st * kQHalfBytes, &tm_w, fb, kk * kPK, nb);
+        issued = kk + 1;
+      }
+      // CTA 0: every copy of the pair that was issued has landed (CTA 1 waits for CTA 0 at the
+      // final cluster barrier, so it cannot exit with copies in flight either)
+      if (rank == 0)
+        for (int kk = issued - kQStages < 0 ? 0 : issued - kQStages; kk < issued; ++kk)
+          mbar_wait(smem_u32(&bars.full[kk % kQStages]), (kk / kQStages) & 1, abort_flag, p.err, 51, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(2 * kPM, kPN, false);
+      const uint64_t da0 = sdesc(sA0, 16, 1024);
+      const uint64_t db0 = sdesc(sB0, 16, 1024);
+      bool ok = true;
+      for (int kk = 0; kk < n_k && ok; ++kk) {
+        const int st = kk % kQStages;
+        const uint32_t par = (kk / kQStages) & 1;
+        ok = __all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.full[st]), par, abort_flag, p.err, 52));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t da = da0 + (uint64_t)((st * kQHalfBytes) >> 4);
+          const uint64_t db = db0 + (uint64_t)((st * kQHalfBytes) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < kPK / 16; ++ks)
+            mma_ss_pair(tmem, da + (uint64_t)((ks * 32) >> 4), db + (uint64_t)((ks * 32) >> 4), idesc,
+                        (kk > 0 || ks > 0) ? 1u : 0u);
+          tc_commit_pair(smem_u32(&bars.empty[st]));
+          if (kk == n_k - 1) tc_commit_pair(smem_u32(&bars.acc_full));
+        }
+        __syncwarp();
+      }
+      if (elect_one()) tc_commit_pair(smem_u32(&bars.drain));
+      __syncwarp();
+    }
+    // neither CTA frees TMEM or exits while the pair's MMAs may still read or write it
+    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 54, false);
+  } else if (warp >= 4) {
+    // token of each of this CTA's rows (-1: past m or past n_tokens: not stored); only the
+    // epilogue reads them, after its CTA-wide barrier
+    const int i = m0 + (int)threadIdx.x - 128;
+    int t = i < p.m ? (p.rows ? p.rows[i] : i) : -1;
+    if (t >= p.n_tokens) t = -1;
+    s_rows[threadIdx.x - 128] = t;
+  }
+
+  proj_epilogue<D>(p, smem_u32(&bars.acc_full), tmem, sA0, s_rows, m0, n0, abort_flag);
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // neither CTA exits while the other may still arrive on its barriers
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols) : "memory");
   }
 }
 
@@ -365,18 +430,33 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 }
 
 template <int D>
-cudaError_t launch_proj_typed(const ProjParams& p, const void* x, const void* w, cudaStream_t s) {
+cudaError_t launch_proj_pair(const ProjParams& p, const void* x, const void* w, cudaStream_t s) {
   const int n_out = (p.hq + 2 * p.hkv) * D;
   CUtensorMap tx, tw;
   if (!encode_2d(&tx, x, (uint64_t)p.d_model, (uint64_t)p.m, kPK, kPM) ||
-      !encode_2d(&tw, w, (uint64_t)p.d_model, (uint64_t)n_out, kPK, kPN))
+      !encode_2d(&tw, w, (uint64_t)p.d_model, (uint64_t)n_out, kPK, kPN / 2))
     return cudaErrorInvalidValue;
-  const size_t smem = 1024 + (size_t)kPStages * (kPABytes + kPBBytes);
+  const size_t smem = 1024 + (size_t)kQStages * 2 * kQHalfBytes;
   static std::atomic<uint64_t> configured{0};
-  const cudaError_t e = set_smem_limit_once(qkv_projection_kernel<D>, (int)smem, configured);
+  const cudaError_t e = set_smem_limit_once(qkv_projection_pair_kernel<D>, (int)smem, configured);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.m + kPM - 1) / kPM, (n_out + kPN - 1) / kPN);
-  return launch_pdl(qkv_projection_kernel<D>, grid, kPThreads, smem, s, tx, tw, p);
+  const int m_tiles = (p.m + kPM - 1) / kPM;
+  const dim3 grid((unsigned)(2 * ((m_tiles + 1) / 2)), (n_out + kPN - 1) / kPN);  // whole pairs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, qkv_projection_pair_kernel<D>, tx, tw, p);
 }
 
 }  // namespace
@@ -409,8 +489,8 @@ cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model
   p.k = static_cast<uint8_t*>(k);
   p.v = static_cast<uint8_t*>(v);
   p.err = err;
-  if (head_dim == 128) return launch_proj_typed<128>(p, a, w, s);
-  if (head_dim == 64) return launch_proj_typed<64>(p, a, w, s);
+  if (head_dim == 128) return launch_proj_pair<128>(p, a, w, s);
+  if (head_dim == 64) return launch_proj_pair<64>(p, a, w, s);
   return cudaErrorInvalidValue;
 }
 
