@@ -34,6 +34,7 @@ ratio-sweep workload.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -945,9 +946,15 @@ def run_diagnostics(args, cfg):
 
 def run_projection(args, cfg):
     """Projection path: per step, the QKV projection (RoPE-encoded q and k) of every layer's
-    recomputed rows, at the blend's row counts (layer 1 all tokens, then C_l and the suffix).
-    Four distinct hidden-state / weight sets (random, of the model's shape) are cycled over the
-    layers, so a layer's weights are not in L2 from the layer before."""
+    recomputed rows, at the blend's row counts: layer 1 all tokens, layer l >= 2 the candidates
+    C_l (= S_{l-1}) and the suffix. A layer's hidden rows are the outputs the previous layer's
+    attention produced, which are exactly its query rows S_{l-1} and the suffix, in that list
+    order; so row i of x is token tokens[i] and the rows are read in place
+    (cb_qkv_projection_indexed with x_index = NULL). The same step with every layer's rows
+    gathered from a full [n_tokens, d_model] matrix (cb_qkv_projection with a row list: the
+    gather kernel plus the GEMM) is timed too and reported under "gathered_rows". Four distinct
+    hidden-state / weight sets (random, of the model's shape) are cycled over the layers, so a
+    layer's weights are not in L2 from the layer before."""
     import torch
     import torch.distributed as dist
 
@@ -967,15 +974,17 @@ def run_projection(args, cfg):
     xs = [bf16_tensor(x, dev) for x, _ in sets]
     ws = [bf16_tensor(w, dev) for _, w in sets]
     rng = np.random.default_rng(cfg.config_id)
-    rows, sizes = [], []
+    tokens, sizes = [], []
+    cand = np.arange(cfg.n_ctx)
     for layer in range(1, cfg.layers + 1):
         n_cand, k, mq, selects = plan.layer_sizes(layer)
         if layer == 1:
             r = np.arange(cfg.n_tokens)  # layer 1 recomputes every token
         else:
-            r = np.concatenate([np.sort(rng.choice(cfg.n_ctx, n_cand, replace=False)),
-                                np.arange(cfg.n_ctx, cfg.n_tokens)])
-        rows.append(torch.as_tensor(r.astype(np.int32), device=dev))
+            if n_cand < cand.size:  # C_l = S_{l-1}: a subset of the previous candidates
+                cand = np.sort(rng.choice(cand, n_cand, replace=False))
+            r = np.concatenate([cand, np.arange(cfg.n_ctx, cfg.n_tokens)])
+        tokens.append(torch.as_tensor(r.astype(np.int32), device=dev))
         sizes.append(r.size)
     d_model = cfg.d_model
     xg = torch.empty((cfg.n_tokens, d_model), dtype=torch.bfloat16, device=dev)
@@ -984,55 +993,71 @@ def run_projection(args, cfg):
     v = torch.empty_like(k)
     stream = torch.cuda.Stream(dev)
 
-    def step():
+    def step_in_place():
         for li in range(cfg.layers):
             s_ = li % len(sets)
-            cb.cb_qkv_projection(plan, xs[s_], rows[li], sizes[li], ws[s_], q, k, v, encode=True, x_gathered=xg,
+            cb.cb_qkv_projection_indexed(plan, xs[s_][: sizes[li]], None, tokens[li], sizes[li], ws[s_], q, k, v,
+                                         encode=True, stream=stream)
+
+    def step_gathered():
+        for li in range(cfg.layers):
+            s_ = li % len(sets)
+            cb.cb_qkv_projection(plan, xs[s_], tokens[li], sizes[li], ws[s_], q, k, v, encode=True, x_gathered=xg,
                                  stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    stream.synchronize()
-    plan.check()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        step()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g.replay()
-    stream.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_index) as clocks:
+    def timed(step, clocked):
         with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(args.steps):
-                g.replay()
-            stop.record(stream)
+            for _ in range(args.warmup):
+                step()
         stream.synchronize()
-    ms = start.elapsed_time(stop) / args.steps
-    plan.check()
-    ms = max_over_ranks(ms, dev, world)
+        plan.check()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        stream.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_index) if clocked else contextlib.nullcontext() as clocks:
+            with torch.cuda.stream(stream):
+                start.record(stream)
+                for _ in range(args.steps):
+                    g.replay()
+                stop.record(stream)
+            stream.synchronize()
+        ms = start.elapsed_time(stop) / args.steps
+        plan.check()
+        return max_over_ranks(ms, dev, world), clocks
+
+    ms, clocks = timed(step_in_place, True)
+    ms_gathered, _ = timed(step_gathered, False)
     n_out = (cfg.hq + 2 * cfg.hkv) * cfg.head_dim
     flops = sum(2.0 * m_ * d_model * n_out for m_ in sizes)
     peaks = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
     tf = flops / (ms * 1e-3) / 1e12
+    tf_g = flops / (ms_gathered * 1e-3) / 1e12
     line = {"metric": "QKV projection TFLOP/s (recomputed rows of every layer)", "value": world * tf,
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1) hidden rows, N(0, 1/d_model) weights of the model's shape",
             "config": {"workload": workload_desc(cfg), "path": "projection", "d_model": d_model, "n_out": n_out,
                        "rows_per_layer": sorted(set(sizes)), "cuda_graph": True,
+                       "rows": "in place: row i of a layer's x is token tokens[i] (the previous layer's "
+                               "attention rows, in list order); layer 1 all tokens",
                        "l2": "four weight sets cycled (4 x %.0f MB)" % (n_out * d_model * 2 / 1e6)},
-            "roofline": {"kernel": "qkv_projection (with the row gather)", "bound": "tensor", "achieved": tf,
-                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                         "frac": tf / peaks["bf16_tflops_sustained"], "traffic": None,
+            "roofline": {"kernel": "qkv_projection_pair", "bound": "tensor", "achieved": tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
                          "peak_source": f"{peaks['source']} bf16 sustained", "flops_per_step": flops},
-            "gpu_launches": 2 * cfg.layers * args.steps, "clocks": clocks.summary()}
+            "gathered_rows": {"ms_per_step": ms_gathered, "achieved": tf_g, "frac": tf_g / peak,
+                              "how": "every layer's rows gathered from a full [n_tokens, d_model] matrix first "
+                                     "(row gather kernel + GEMM per layer)"},
+            "gpu_launches": cfg.layers * args.steps, "clocks": clocks.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()

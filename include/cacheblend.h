@@ -207,6 +207,20 @@ cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_
                             int32_t m, const void* w_qkv, int32_t encode, void* x_gathered, void* q, void* k, void* v,
                             void* stream);
 
+/* The same projection with the row of x and the token written given separately (the layout of a
+ * layer-by-layer pass, "rag的kvcache问题" §渐进式过滤机制: the hidden rows a layer passes on are those
+ * of the tokens it recomputed, in its list order, so the next layer reads them in place when its
+ * set is the same, and by position in that list when its set is a subset):
+ *   y_i = x[x_index ? x_index[i] : i] W^T,  written (and RoPE-encoded) at token
+ *   t_i = tokens ? tokens[i] : i,  i in [0, m).
+ * cb_qkv_projection(rows) is x_index = tokens = rows. With x_index, x_gathered (caller-owned,
+ * [m, d_model] bf16) receives the gathered rows first; without it x[0 .. m) is read in place
+ * (m <= x_rows). Without tokens, m <= n_tokens. An index outside x, or a token outside the plan's
+ * n_tokens, is recorded as CB_ERR_DEVICE_CHECK and that row is not written. */
+cb_status cb_qkv_projection_indexed(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model,
+                                    const int32_t* x_index, const int32_t* tokens, int32_t m, const void* w_qkv,
+                                    int32_t encode, void* x_gathered, void* q, void* k, void* v, void* stream);
+
 /* Decode attention over a cache ("rag的kvcache问题" §阶段 2 (Decode): after the prefill the
  * newest token is the only query, and its [1, d] query row is matched against the whole
  * cached K/V, which makes the step memory-bound). For the newest token at position

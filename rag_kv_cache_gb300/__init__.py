@@ -17,7 +17,7 @@ from ._lib import CacheBlendError, check
 
 __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb_kv_deviation_kv", "cb_hkvd_topk",
            "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_attention_sparsity",
-           "cb_output_deviation", "cb_qkv_projection", "cb_blend_layer", "cb_blend_stage",
+           "cb_output_deviation", "cb_qkv_projection", "cb_qkv_projection_indexed", "cb_blend_layer", "cb_blend_stage",
            "cb_blend_request", "cb_hkvd_select_noalloc", "cb_attention_uses_paired_tiles",
            "cb_test_attention_wait_timeout", "cb_check", "cb_version",
            "LayerBuffers"]
@@ -184,6 +184,17 @@ def cb_qkv_projection(plan, x, rows, m, w_qkv, q, k, v, encode=False, x_gathered
         plan.handle, _ptr(x, torch.bfloat16, "x"), x.shape[0], x.shape[1], _ptr(rows, torch.int32, "rows"), m,
         _ptr(w_qkv, torch.bfloat16, "w_qkv"), 1 if encode else 0, _ptr(x_gathered, torch.bfloat16, "x_gathered"),
         _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"), _stream(stream)))
+
+
+def cb_qkv_projection_indexed(plan, x, x_index, tokens, m, w_qkv, q, k, v, encode=False, x_gathered=None,
+                              stream=None):
+    """q / k / v at tokens[i] (int32, or None: token i) from x[x_index[i]] W^T (x_index int32, or
+    None: x[i] read in place), RoPE-encoded q and k when `encode` (see cacheblend.h)."""
+    check(_lib.load().cb_qkv_projection_indexed(
+        plan.handle, _ptr(x, torch.bfloat16, "x"), x.shape[0], x.shape[1], _ptr(x_index, torch.int32, "x_index"),
+        _ptr(tokens, torch.int32, "tokens"), m, _ptr(w_qkv, torch.bfloat16, "w_qkv"), 1 if encode else 0,
+        _ptr(x_gathered, torch.bfloat16, "x_gathered"), _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+        _ptr(v, torch.bfloat16, "v"), _stream(stream)))
 
 
 def cb_hkvd_select_noalloc(v_new, v_old, cand, m, k, n_rows, sel_tok, sel_row, stream=None):

@@ -25,7 +25,7 @@ STAGES = {"deviation": 0, "topk": 1, "fuse": 2, "attention": 3}  # cb_stage
 # every symbol include/cacheblend.h declares
 EXPORTS = ("cb_plan_create", "cb_plan_destroy", "cb_layer_sizes", "cb_rope_rerotate", "cb_kv_deviation",
            "cb_kv_deviation_kv", "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention",
-           "cb_attention_sparsity", "cb_output_deviation", "cb_qkv_projection",
+           "cb_attention_sparsity", "cb_output_deviation", "cb_qkv_projection", "cb_qkv_projection_indexed",
            "cb_blend_layer", "cb_blend_stage", "cb_blend_request", "cb_hkvd_select_noalloc",
            "cb_attention_uses_paired_tiles", "cb_test_attention_wait_timeout", "cb_check",
            "cb_last_error_string", "cb_version")
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cb_attention_sparsity": (i32, [vp, vp, vp, i32, vp, vp, i32, f32, f32, vp, vp, vp, vp, vp]),
         "cb_output_deviation": (i32, [vp, vp, vp, i32, vp, vp]),
         "cb_qkv_projection": (i32, [vp, vp, i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp]),
+        "cb_qkv_projection_indexed": (i32, [vp, vp, i32, i32, vp, vp, i32, vp, i32, vp, vp, vp, vp, vp]),
         "cb_blend_layer": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), vp]),
         "cb_blend_stage": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), i32, vp]),
         "cb_blend_request": (i32, [vp, i32, ctypes.POINTER(CbLayerIO), vp]),

@@ -409,28 +409,43 @@ cb_status cb_output_deviation(cb_plan* plan, const void* o, const void* o_ref, i
                      "cb_output_deviation");
 }
 
-cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows,
-                            int32_t m, const void* w_qkv, int32_t encode, void* x_gathered, void* q, void* k, void* v,
-                            void* stream) {
-  CB_NVTX_RANGE();
+static cb_status qkv_projection(const char* fn, cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model,
+                                const int32_t* x_index, const int32_t* tokens, int32_t m, const void* w_qkv,
+                                int32_t encode, void* x_gathered, void* q, void* k, void* v, void* stream) {
   CB_TRY(check_plan(plan));
   if (m < 0 || x_rows < 0) return fail(CB_ERR_INVALID_ARG, "negative size");
   if (m == 0) return CB_OK;
   if (!cb::qkv_projection_supported(d_model))
     return fail(CB_ERR_UNSUPPORTED, "d_model %d: a positive multiple of 64 is required", d_model);
-  if (rows == nullptr && m > x_rows) return fail(CB_ERR_INVALID_ARG, "m > x_rows without a row list");
-  if (rows == nullptr && m > plan->n_tokens) return fail(CB_ERR_INVALID_ARG, "m > n_tokens without a row list");
+  if (x_index == nullptr && m > x_rows) return fail(CB_ERR_INVALID_ARG, "m > x_rows without an index list");
+  if (tokens == nullptr && m > plan->n_tokens) return fail(CB_ERR_INVALID_ARG, "m > n_tokens without a token list");
   CB_TRY(need_tensor(x, "x"));
   CB_TRY(need_tensor(w_qkv, "w_qkv"));
   CB_TRY(need_tensor(q, "q"));
   CB_TRY(need_tensor(k, "k"));
   CB_TRY(need_tensor(v, "v"));
-  if (rows != nullptr) CB_TRY(need_tensor(x_gathered, "x_gathered"));
+  if (x_index != nullptr) CB_TRY(need_tensor(x_gathered, "x_gathered"));
   const auto& c = plan->cfg;
-  return cuda_status(cb::launch_qkv_projection(x, x_rows, d_model, rows, m, x_gathered, w_qkv, plan->n_tokens, c.hq,
-                                               c.hkv, c.head_dim, encode ? 1 : 0, c.rope_style, table(plan), q, k, v,
-                                               plan->err, static_cast<cudaStream_t>(stream)),
-                     "cb_qkv_projection");
+  return cuda_status(cb::launch_qkv_projection(x, x_rows, d_model, x_index, tokens, m, x_gathered, w_qkv,
+                                               plan->n_tokens, c.hq, c.hkv, c.head_dim, encode ? 1 : 0, c.rope_style,
+                                               table(plan), q, k, v, plan->err, static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+cb_status cb_qkv_projection(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows,
+                            int32_t m, const void* w_qkv, int32_t encode, void* x_gathered, void* q, void* k, void* v,
+                            void* stream) {
+  CB_NVTX_RANGE();
+  return qkv_projection("cb_qkv_projection", plan, x, x_rows, d_model, rows, rows, m, w_qkv, encode, x_gathered, q,
+                        k, v, stream);
+}
+
+cb_status cb_qkv_projection_indexed(cb_plan* plan, const void* x, int32_t x_rows, int32_t d_model,
+                                    const int32_t* x_index, const int32_t* tokens, int32_t m, const void* w_qkv,
+                                    int32_t encode, void* x_gathered, void* q, void* k, void* v, void* stream) {
+  CB_NVTX_RANGE();
+  return qkv_projection("cb_qkv_projection_indexed", plan, x, x_rows, d_model, x_index, tokens, m, w_qkv, encode,
+                        x_gathered, q, k, v, stream);
 }
 
 cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,

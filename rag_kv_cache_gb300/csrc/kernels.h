@@ -142,13 +142,14 @@ cudaError_t launch_decode_attention(const void* q, const void* k, const void* v,
                                     int32_t hkv, int32_t head_dim, float scale, void* out, const DecodeScratch& ws,
                                     cudaStream_t s);
 
-// QKV projection of gathered rows (rows null: row i is token i, read from x directly; else the
-// rows are first copied to x_gathered [m, d_model]): q / k / v rows of token t = rows[i] from
-// x[t] W^T, q and k RoPE-encoded at position t when `encode`. W: [(hq + 2 hkv) head_dim, d_model].
-cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows, int32_t m,
-                                  void* x_gathered, const void* w, int32_t n_tokens, int32_t hq, int32_t hkv,
-                                  int32_t head_dim, int32_t encode, int32_t style, RopeTable t, void* q, void* k,
-                                  void* v, int32_t* err, cudaStream_t s);
+// QKV projection of listed rows: q / k / v rows of token t_i = tokens[i] (null: i) from
+// x[x_index[i]] W^T (x_index null: x[i], read in place; else the rows are first copied to
+// x_gathered [m, d_model]), q and k RoPE-encoded at position t_i when `encode`.
+// W: [(hq + 2 hkv) head_dim, d_model].
+cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* x_index,
+                                  const int32_t* tokens, int32_t m, void* x_gathered, const void* w, int32_t n_tokens,
+                                  int32_t hq, int32_t hkv, int32_t head_dim, int32_t encode, int32_t style, RopeTable t,
+                                  void* q, void* k, void* v, int32_t* err, cudaStream_t s);
 bool qkv_projection_supported(int32_t d_model);
 
 }  // namespace cb

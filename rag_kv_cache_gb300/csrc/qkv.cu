@@ -3,14 +3,15 @@
 // projection weights, computed as one product of the stacked rows; §渐进式过滤机制: a layer
 // recomputes only its candidate tokens and the query suffix).
 //
-//   y[i, :] = x[rows[i], :] W^T,  W = W_qkv [(Hq + 2 Hkv) D, d_model] (one output feature per row)
-//   q[t] = y[i, Q heads], k[t] = y[i, K heads], v[t] = y[i, V heads],  t = rows[i],
+//   y[i, :] = x[x_index[i], :] W^T,  W = W_qkv [(Hq + 2 Hkv) D, d_model] (one output feature per row)
+//   q[t] = y[i, Q heads], k[t] = y[i, K heads], v[t] = y[i, V heads],  t = tokens[i],
 // with q and k optionally RoPE-encoded at position t (the plan's cos/sin table) in the epilogue,
 // all written token-indexed as bf16: the layout the blend reads its recomputed rows from.
 //
-// The candidate rows of X are first gathered into a contiguous workspace by a streaming kernel
-// (2 m d_model bytes each way): a 128-byte-swizzled TMA tile must land on a 1024-byte boundary,
-// which four-row gathers into one tile cannot all meet. A cluster of two CTAs then computes a
+// (x_index null: row i of x; tokens null: token i). With an index list the rows of X are first
+// gathered into a contiguous workspace by a streaming kernel (2 m d_model bytes each way): a
+// 128-byte-swizzled TMA tile must land on a 1024-byte boundary, which four-row gathers into one
+// tile cannot all meet; without one the tiles read x in place. A cluster of two CTAs then computes a
 // 256 x 256 output tile with tcgen05 cta_group::2: CTA r holds 128 gathered rows and W rows
 // n0 + 128 r .. n0 + 128 r + 127 of the tile's 256 output features (two 128-wide heads or four
 // 64-wide heads of one of Q, K, V), and the pair's MMA (M 256, N 256, K 16; bf16 in, fp32
@@ -47,7 +48,7 @@ constexpr int kPThreads = 256;
 constexpr uint32_t kPTmemCols = 256;
 
 struct ProjParams {
-  const int32_t* rows;  // token id of row i (null: row i is token i)
+  const int32_t* tokens;  // token of output row i (null: token i)
   int m;
   int n_tokens;
   int d_model;
@@ -390,11 +391,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // neither CTA frees TMEM or exits while the pair's MMAs may still read or write it
     mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 54, false);
   } else if (warp >= 4) {
-    // token of each of this CTA's rows (-1: past m or past n_tokens: not stored); only the
+    // token of each of this CTA's rows (-1: past m, or outside the cache: not stored); only the
     // epilogue reads them, after its CTA-wide barrier
     const int i = m0 + (int)threadIdx.x - 128;
-    int t = i < p.m ? (p.rows ? p.rows[i] : i) : -1;
-    if (t >= p.n_tokens) t = -1;
+    int t = -1;
+    if (i < p.m) {
+      t = p.tokens ? p.tokens[i] : i;
+      if (t < 0 || t >= p.n_tokens) {
+        if (blockIdx.y == 0) record_error(p.err, kErrIndex, i);  // once per row
+        t = -1;
+      }
+    }
     s_rows[threadIdx.x - 128] = t;
   }
 
@@ -461,21 +468,21 @@ cudaError_t launch_proj_pair(const ProjParams& p, const void* x, const void* w, 
 
 }  // namespace
 
-cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* rows, int32_t m,
-                                  void* x_gathered, const void* w, int32_t n_tokens, int32_t hq, int32_t hkv,
-                                  int32_t head_dim, int32_t encode, int32_t style, RopeTable t, void* q, void* k,
-                                  void* v, int32_t* err, cudaStream_t s) {
+cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model, const int32_t* x_index,
+                                  const int32_t* tokens, int32_t m, void* x_gathered, const void* w, int32_t n_tokens,
+                                  int32_t hq, int32_t hkv, int32_t head_dim, int32_t encode, int32_t style, RopeTable t,
+                                  void* q, void* k, void* v, int32_t* err, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
   const void* a = x;
-  if (rows != nullptr) {  // gather the rows into the workspace first
+  if (x_index != nullptr) {  // gather the rows into the workspace first
     const int blocks = (int)(((int64_t)m * 32 + 255) / 256);
     const cudaError_t e = launch_pdl(gather_rows_kernel, blocks, 256, 0, s, (uint8_t*)x_gathered, (const uint8_t*)x,
-                                     rows, m, x_rows, d_model * 2, err);
+                                     x_index, m, x_rows, d_model * 2, err);
     if (e != cudaSuccess) return e;
     a = x_gathered;
   }
   ProjParams p;
-  p.rows = rows;
+  p.tokens = tokens;
   p.m = m;
   p.n_tokens = n_tokens;
   p.d_model = d_model;

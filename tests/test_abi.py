@@ -64,3 +64,6 @@ def test_host_validation_without_gpu(lib_path):
     assert lib.cb_rope_rerotate(None, None, None, None, None, None, None, 1, 1, 1, 1, None) == 1
     assert lib.cb_blend_layer(None, 1, None, None) == 1
     assert lib.cb_check(None) == 1
+    # a projection call without a plan is refused before any argument is read
+    assert lib.cb_qkv_projection_indexed(None, None, 0, 64, None, None, 1, None, 0, None, None, None, None, None) == 1
+    assert b"plan" in lib.cb_last_error_string()

@@ -122,3 +122,72 @@ def test_gathered_rows_repeat_bit_identical(cb):
     plan.check()
     assert not torch.equal(first[0], first[1])
     plan.close()
+
+
+def _run_indexed(cb, cfg, x_full, w, x_in, x_index, tokens, encode=True):
+    """cb_qkv_projection_indexed on x_in (rows x_in[x_index[i]] or x_in[i]) written at tokens; the
+    oracle takes the same hidden rows from x_full, where x_full[tokens[i]] is that row."""
+    plan = cb.Plan.from_config(cfg)
+    n, m = cfg.n_tokens, len(tokens)
+    sentinel = lambda h: torch.full((n, h, cfg.head_dim), 7.0, dtype=torch.bfloat16, device="cuda")
+    q, k, v = sentinel(cfg.hq), sentinel(cfg.hkv), sentinel(cfg.hkv)
+    xg = torch.empty((m, x_in.shape[1]), dtype=torch.bfloat16, device="cuda") if x_index is not None else None
+    cb.cb_qkv_projection_indexed(plan, bf16_tensor(x_in), None if x_index is None else _i32(x_index), _i32(tokens), m,
+                                 bf16_tensor(w), q, k, v, encode=encode, x_gathered=xg)
+    plan.check()
+    plan.close()
+    tok = np.asarray(tokens)
+    oq, ok, ov = qkv_projection(bf16_bits_to_f64(x_full), tok, bf16_bits_to_f64(w), cfg.hq, cfg.hkv, cfg.head_dim,
+                                cfg.rope_theta, encode, "half")
+    got = [bf16_bits_to_f64(bf16_bits(t)) for t in (q, k, v)]
+    for g, o, what in zip(got, (oq, ok, ov), "qkv"):
+        assert_close_bf16(g[tok], o, what=what)
+        assert np.all(g[np.setdiff1d(np.arange(n), tok)] == 7.0)
+
+
+def test_indexed_rows_in_place_written_at_tokens(cb):
+    # Layers 4.. of the kept set: the previous layer left the hidden rows of S and the suffix in
+    # list order, so row i of x is token tokens[i] (Mistral-7B shape, 460 + 64 rows).
+    cfg = get_config("mistral7b")
+    x, w = generate_projection(cfg, 3)
+    rng = np.random.default_rng(46)
+    tokens = np.concatenate([np.sort(rng.choice(cfg.n_ctx, 460, replace=False)), np.arange(cfg.n_ctx, cfg.n_tokens)])
+    _run_indexed(cb, cfg, x, w, x[tokens], None, tokens)
+
+
+def test_indexed_rows_by_position_in_a_compact_list(cb):
+    # Layer 3 of the kept set: x holds the rows of the candidate list C (and the suffix) in list
+    # order; S is a subset, taken by position. Unsorted positions, tiny shape with a 256-wide model.
+    cfg = get_config("tiny")
+    x, w = generate_projection(cfg, 4)
+    rng = np.random.default_rng(47)
+    cand = np.concatenate([np.sort(rng.choice(cfg.n_ctx, 150, replace=False)), np.arange(cfg.n_ctx, cfg.n_tokens)])
+    pos = rng.permutation(cand.size)[:90]
+    _run_indexed(cb, cfg, x, w, x[cand], pos, cand[pos])
+
+
+def test_indexed_bad_index_and_token_are_recorded(cb):
+    cfg = get_config("tiny")
+    plan = cb.Plan.from_config(cfg)
+    x, w = generate_projection(cfg, 1)
+    q = torch.zeros((cfg.n_tokens, cfg.hq, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((cfg.n_tokens, cfg.hkv, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    xg = torch.empty((3, x.shape[1]), dtype=torch.bfloat16, device="cuda")
+    xd, wd = bf16_tensor(x[:10]), bf16_tensor(w)
+    # a token outside the plan: recorded, that row not written, the others written
+    cb.cb_qkv_projection_indexed(plan, xd, None, _i32([4, cfg.n_tokens, 6]), 3, wd, q, k, v)
+    with pytest.raises(cb.CacheBlendError):
+        plan.check()
+    assert torch.count_nonzero(q[4]) > 0 and torch.count_nonzero(q[6]) > 0
+    plan.close()
+    plan = cb.Plan.from_config(cfg)
+    q.zero_()
+    # an index outside x: recorded
+    cb.cb_qkv_projection_indexed(plan, xd, _i32([1, 10, 2]), _i32([4, 5, 6]), 3, wd, q, k, v, x_gathered=xg)
+    with pytest.raises(cb.CacheBlendError):
+        plan.check()
+    assert torch.count_nonzero(q[4]) > 0 and torch.count_nonzero(q[6]) > 0
+    with pytest.raises(cb.CacheBlendError):  # in place needs m <= x_rows
+        cb.cb_qkv_projection_indexed(plan, xd, None, None, 11, wd, q, k, v)
+    plan.close()
