@@ -228,10 +228,12 @@ cb_status cb_qkv_projection_indexed(cb_plan* plan, const void* x, int32_t x_rows
  *   out[h] = sum_{j < n_keys} softmax_j(scale * q[h] . k[j, g]) v[j, g],  g = h / (hq/hkv),
  * q, out: [hq, D] (q RoPE-encoded at n_keys - 1); k, v: [n_keys, hkv, D], key j at
  * position j (e.g. a layer's k_fused / v_fused with the new token appended). scale <= 0
- * selects 1/sqrt(D). fp32 dot products and softmax on the CUDA cores, bf16 output. The keys
- * of each kv head are split over up to 40 CTAs whose partial results meet in the plan's
- * decode scratch (the last CTA of a kv head merges them), so decode calls on one plan must
- * not overlap on the GPU: order them on one stream, or give each stream its own plan. */
+ * selects 1/sqrt(D). Both products run on the tensor cores (bf16 in, fp32 accumulate; the
+ * softmax weights rounded to bf16 before P V, as in cb_hkvd_attention); bf16 output. The keys
+ * of each kv head are split over up to 40 CTAs (one wave over all kv heads) whose partial
+ * results meet in the plan's decode scratch (the last CTA of a kv head merges them), so decode
+ * calls on one plan must not overlap on the GPU: order them on one stream, or give each stream
+ * its own plan. A bounded wait that gives up records CB_ERR_TIMEOUT in the plan's error word. */
 cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
                               float scale, void* out, void* stream);
 

@@ -460,8 +460,10 @@ cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const
   CB_TRY(need_tensor(out, "out"));
   const auto& c = plan->cfg;
   if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)c.head_dim);
-  return cuda_status(cb::launch_decode_attention(q, k, v, n_keys, c.hq, c.hkv, c.head_dim, scale, out, plan->decode,
-                                                 static_cast<cudaStream_t>(stream)),
+  if (!cb::decode_tc_supported(c.hq, c.hkv, c.head_dim))
+    return fail(CB_ERR_UNSUPPORTED, "decode: hq / hkv = %d, head_dim %d", c.hq / c.hkv, c.head_dim);
+  return cuda_status(cb::launch_decode_tc(q, k, v, n_keys, c.hq, c.hkv, c.head_dim, scale, out, plan->decode,
+                                          plan->err, static_cast<cudaStream_t>(stream)),
                      "cb_decode_attention");
 }
 

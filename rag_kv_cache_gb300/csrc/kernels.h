@@ -132,15 +132,18 @@ struct DecodeScratch {
   float* part_o;      // [hkv][decode_max_splits()][G][D]
   float2* part_ml;    // [hkv][decode_max_splits()][G]
   int32_t* tickets;   // [hkv]
-  int32_t target_ctas;  // CTAs to aim for over all kv heads (two per SM)
+  int32_t target_ctas;  // twice the SM count (the launch takes one CTA per SM)
 };
 
 int32_t decode_max_splits();
 
-// Decode attention: one query row q [hq, D] over the whole cache k, v [n_keys, hkv, D].
-cudaError_t launch_decode_attention(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq,
-                                    int32_t hkv, int32_t head_dim, float scale, void* out, const DecodeScratch& ws,
-                                    cudaStream_t s);
+// Decode attention on the tensor cores: one query row q [hq, D] over the whole cache k, v
+// [n_keys, hkv, D] (head_dim 64 or 128, at most 32 query heads per kv head); `err` receives a
+// timeout of one of its bounded waits.
+bool decode_tc_supported(int32_t hq, int32_t hkv, int32_t head_dim);
+cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq, int32_t hkv,
+                             int32_t head_dim, float scale, void* out, const DecodeScratch& ws, int32_t* err,
+                             cudaStream_t s);
 
 // QKV projection of listed rows: q / k / v rows of token t_i = tokens[i] (null: i) from
 // x[x_index[i]] W^T (x_index null: x[i], read in place; else the rows are first copied to
