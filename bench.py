@@ -821,7 +821,7 @@ def run_decode(args, cfg):
             "config": {"workload": workload_desc(cfg), "path": "decode", "n_keys": n_keys,
                        "l2": f"inputs larger than L2: {cfg.layers * bytes_launch / 1e9:.2f} GB per step",
                        "cuda_graph": True},
-            "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+            "roofline": {"kernel": "decode_tc", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
                          "peak_source": f"{peaks['source']} copy bandwidth", "bytes_per_launch": bytes_launch,
                          "launches_per_step": cfg.layers, "avg_launch_us": us_launch},
