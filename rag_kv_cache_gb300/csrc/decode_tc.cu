@@ -55,7 +55,7 @@ struct TcBars {
 
 struct TcParams {
   int n_keys;
-  int hq, hkv, G;
+  int G;  // query heads per kv head
   int tiles_per_split;
   int n_tiles;      // key tiles in all
   float scale_log2;
@@ -446,8 +446,6 @@ cudaError_t launch_decode_tc_t(const void* q, const void* k, const void* v, int3
   const int splits = (n_tiles + per - 1) / per;  // every split has at least one tile
   TcParams p;
   p.n_keys = n_keys;
-  p.hq = hq;
-  p.hkv = hkv;
   p.G = G;
   p.tiles_per_split = per;
   p.n_tiles = n_tiles;

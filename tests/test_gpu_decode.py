@@ -44,7 +44,7 @@ def _check(cb, plan, q, k, v, n_keys, scale=0.0, what="decode"):
 
 @pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (32, 8, 128), (64, 8, 128), (16, 16, 128), (32, 16, 64),
                                       (16, 1, 64), (32, 2, 128)])
-@pytest.mark.parametrize("n_keys", [1, 7, 9, 33, 300, 3137])
+@pytest.mark.parametrize("n_keys", [1, 7, 9, 33, 127, 128, 129, 256, 300, 3137])
 def test_decode_shapes_and_lengths(cb, hq, hkv, d, n_keys):
     rng = np.random.default_rng(hq * 1000 + hkv * 10 + n_keys)
     plan = _plan(cb, hq, hkv, d)
