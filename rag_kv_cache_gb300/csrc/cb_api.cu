@@ -149,7 +149,7 @@ cb_status cb_plan_create(const cb_config* cfg, cb_plan** out) {
   if (e == cudaSuccess) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
-    p->decode.target_ctas = 2 * (sms > 0 ? sms : 1);
+    p->decode.sms = sms > 0 ? sms : 1;
   }
   const size_t dec_units = (size_t)c.hq * cb::decode_max_splits();  // (kv head, split, q head) triples
   if (e == cudaSuccess) e = cudaMalloc(&p->decode.part_o, sizeof(float) * dec_units * c.head_dim);

@@ -438,7 +438,7 @@ cudaError_t launch_decode_tc_t(const void* q, const void* k, const void* v, int3
       return cudaErrorInvalidValue;
   }
   const int n_tiles = (n_keys + kTBN - 1) / kTBN;
-  const int sms = ws.target_ctas / 2 > 0 ? ws.target_ctas / 2 : 1;
+  const int sms = ws.sms > 0 ? ws.sms : 1;
   int max_splits = sms / hkv;
   if (max_splits > kTMaxSplits) max_splits = kTMaxSplits;
   if (max_splits < 1) max_splits = 1;

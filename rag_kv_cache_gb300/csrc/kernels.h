@@ -132,7 +132,7 @@ struct DecodeScratch {
   float* part_o;      // [hkv][decode_max_splits()][G][D]
   float2* part_ml;    // [hkv][decode_max_splits()][G]
   int32_t* tickets;   // [hkv]
-  int32_t target_ctas;  // twice the SM count (the launch takes one CTA per SM)
+  int32_t sms;        // the device's SM count (the launch takes one CTA per SM, one wave)
 };
 
 int32_t decode_max_splits();
