@@ -369,6 +369,19 @@ int32_t cb_attention_uses_paired_tiles(const cb_plan* plan, int32_t mq);
 cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq,
                                          const void* k, const void* v, int32_t n_keys, void* out, void* stream);
 
+/* Test support for the failure path, not part of the blend (the pages have no
+ * counterpart). Runs cb_decode_attention's kernel (head_dim 128 only) in a form
+ * whose producer never copies key tile 1 of its split and whose bounded waits
+ * give up after 100 us instead of 2 s: every CTA with a second key tile records
+ * CB_ERR_TIMEOUT in the plan's error word, skips the rest of its tiles, waits
+ * (again bounded) for its own copies and tensor-core work, frees its tensor
+ * memory and still takes its ticket, so the split counters stay consistent; the
+ * contents of `out` are undefined. The next cb_check reports CB_ERR_TIMEOUT and
+ * clears the word, and the device and the plan stay usable. Arguments as
+ * cb_decode_attention (scale 1/sqrt(D)); CB_ERR_INVALID_ARG if n_keys <= 128. */
+cb_status cb_test_decode_wait_timeout(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
+                                      void* out, void* stream);
+
 /* Synchronise the plan's device, read and clear its error word. Returns
  * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
  * cb_last_error_string). Off the hot path. */

@@ -357,6 +357,22 @@ cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int
                      "cb_test_attention_wait_timeout");
 }
 
+cb_status cb_test_decode_wait_timeout(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
+                                      void* out, void* stream) {
+  CB_NVTX_RANGE();
+  CB_TRY(check_plan(plan));
+  if (plan->cfg.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "the wait-timeout probe needs head_dim 128");
+  if (n_keys <= 128) return fail(CB_ERR_INVALID_ARG, "the wait-timeout probe needs n_keys > 128");
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  CB_TRY(need_tensor(out, "out"));
+  const auto& c = plan->cfg;
+  return cuda_status(cb::launch_decode_timeout_probe(q, k, v, n_keys, c.hq, c.hkv, 1.0f / std::sqrt(128.0f), out,
+                                                     plan->decode, plan->err, static_cast<cudaStream_t>(stream)),
+                     "cb_test_decode_wait_timeout");
+}
+
 cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
                                 const void* v, int32_t n_keys, float scale, float eps, void* out, void* row_stats,
                                 int32_t* counts, uint64_t* total, void* stream) {

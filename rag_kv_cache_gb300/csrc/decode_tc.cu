@@ -70,7 +70,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int D>
+// PROBE: the wait-timeout probe (test support only): the producer arms key tile 1's barrier of
+// every CTA but never copies the tile, and every wait gives up after kProbeTimeoutNs, so each CTA
+// that has a second tile takes its failure path (timeout recorded, copies and tensor-core work
+// drained, TMEM freed; the ticket is still taken, so the counters stay consistent).
+template <int D, bool PROBE = false>
 __global__ void __launch_bounds__(kTThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -80,6 +84,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   constexpr uint32_t kQBytes = kBoxes * kQBox;
   constexpr uint32_t kKVBytes = kBoxes * kKVBox;
   constexpr uint32_t kColO = 256;
+  constexpr uint64_t kLimit = PROBE ? kProbeTimeoutNs : kTimeoutNs;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ TcBars bars;
@@ -154,24 +159,27 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const int st = j % kTStages;
         if (j >= kTStages) {
           const uint32_t par = ((j / kTStages) - 1) & 1;
-          if (!mbar_spin(smem_u32(&bars.k_free[st]), par, abort_flag, p.err, 60)) break;
-          if (!mbar_spin(smem_u32(&bars.pv_done[st]), par, abort_flag, p.err, 61)) break;
+          if (!mbar_spin(smem_u32(&bars.k_free[st]), par, abort_flag, p.err, 60, kLimit)) break;
+          if (!mbar_spin(smem_u32(&bars.pv_done[st]), par, abort_flag, p.err, 61, kLimit)) break;
         }
         const int key0 = (j0 + j) * kTBN;  // past n_keys: zero fill
         const uint32_t kb = smem_u32(&bars.k_full[st]), vb = smem_u32(&bars.v_full[st]);
         mbar_expect_tx(kb, kKVBytes);
+        if (!(PROBE && j == 1)) {  // the probe never copies key tile 1: its barrier cannot complete
 #pragma unroll
-        for (int b = 0; b < kBoxes; ++b) tma_load_3d(sK0 + st * kKVBytes + b * kKVBox, &tm_k, kb, b * 64, g, key0);
+          for (int b = 0; b < kBoxes; ++b)
+            tma_load_3d(sK0 + st * kKVBytes + b * kKVBox, &tm_k, kb, b * 64, g, key0);
+        }
         mbar_expect_tx(vb, kKVBytes);
 #pragma unroll
         for (int b = 0; b < kBoxes; ++b) tma_load_3d(sV0 + st * kKVBytes + b * kKVBox, &tm_v, vb, b * 64, g, key0);
         nk = j + 1;
       }
       // every copy issued has landed before the CTA may exit
-      mbar_wait(qb, 0, abort_flag, p.err, 62, false);
+      mbar_wait(qb, 0, abort_flag, p.err, 62, false, kLimit);
       for (int j = nk - kTStages < 0 ? 0 : nk - kTStages; j < nk; ++j) {
-        mbar_wait(smem_u32(&bars.k_full[j % kTStages]), (j / kTStages) & 1, abort_flag, p.err, 63, false);
-        mbar_wait(smem_u32(&bars.v_full[j % kTStages]), (j / kTStages) & 1, abort_flag, p.err, 64, false);
+        mbar_wait(smem_u32(&bars.k_full[j % kTStages]), (j / kTStages) & 1, abort_flag, p.err, 63, false, kLimit);
+        mbar_wait(smem_u32(&bars.v_full[j % kTStages]), (j / kTStages) & 1, abort_flag, p.err, 64, false, kLimit);
       }
     }
     __syncwarp();
@@ -182,7 +190,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const uint64_t dk0 = sdesc(sK0, 16, 1024);
     const uint64_t dv0 = sdesc(sV0, kKVBox, 1024);
     auto spin_all = [&](uint32_t bar, uint32_t parity, int site) -> bool {
-      return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site));
+      return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site, kLimit));
     };
     // S_j = Q K_j^T into buffer j % 2; its commit frees the K stage and hands S_j to the softmax.
     auto issue_s = [&](int j) -> bool {
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     // every MMA issued here completes before TMEM is freed
     if (elect_one()) tc_commit(smem_u32(&bars.drain));
     __syncwarp();
-    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 69, false);
+    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 69, false, kLimit);
   }
 
   // Softmax (warp 4, one thread per head row) and the CTA's partial result.
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const uint32_t lanes = tmem;  // warp 4 reads TMEM lanes 0-31
   if (warp == kWarpSoftmax) {
     auto wait_all = [&](uint32_t bar, uint32_t parity, int site) -> bool {
-      return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site));
+      return __all_sync(0xffffffffu, mbar_spin(bar, parity, abort_flag, p.err, site, kLimit));
     };
     for (int j = 0; j < n && ok; ++j) {
       const int b = j & 1;
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool PROBE = false>
 cudaError_t launch_decode_tc_t(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq, int32_t hkv,
                                float scale, void* out, const DecodeScratch& ws, int32_t* err, cudaStream_t s) {
   const int G = hq / hkv;
@@ -457,9 +465,9 @@ cudaError_t launch_decode_tc_t(const void* q, const void* k, const void* v, int3
   p.err = err;
   const size_t smem = 1024 + (size_t)(D / 64) * (kTBM * 128 + 2 * kTStages * kTBN * 128);
   static std::atomic<uint64_t> configured{0};
-  const cudaError_t e = set_smem_limit_once(decode_tc_kernel<D>, (int)smem, configured);
+  const cudaError_t e = set_smem_limit_once(decode_tc_kernel<D, PROBE>, (int)smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<D>, dim3(splits, hkv), dim3(kTThreads), smem, s, tq, tk, tv, p);
+  return launch_pdl(decode_tc_kernel<D, PROBE>, dim3(splits, hkv), dim3(kTThreads), smem, s, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -477,6 +485,13 @@ cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int32_
   if (head_dim == 128) return launch_decode_tc_t<128>(q, k, v, n_keys, hq, hkv, scale, out, ws, err, s);
   if (head_dim == 64) return launch_decode_tc_t<64>(q, k, v, n_keys, hq, hkv, scale, out, ws, err, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_timeout_probe(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq,
+                                        int32_t hkv, float scale, void* out, const DecodeScratch& ws, int32_t* err,
+                                        cudaStream_t s) {
+  if (n_keys <= kTBN) return cudaErrorInvalidValue;  // no key tile 1 to miss
+  return launch_decode_tc_t<128, true>(q, k, v, n_keys, hq, hkv, scale, out, ws, err, s);
 }
 
 }  // namespace cb

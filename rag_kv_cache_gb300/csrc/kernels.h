@@ -144,6 +144,11 @@ bool decode_tc_supported(int32_t hq, int32_t hkv, int32_t head_dim);
 cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq, int32_t hkv,
                              int32_t head_dim, float scale, void* out, const DecodeScratch& ws, int32_t* err,
                              cudaStream_t s);
+// Test support: the same kernel (head_dim 128) in a form whose key tile 1 never arrives and whose
+// waits give up after kProbeTimeoutNs (n_keys > 128).
+cudaError_t launch_decode_timeout_probe(const void* q, const void* k, const void* v, int32_t n_keys, int32_t hq,
+                                        int32_t hkv, float scale, void* out, const DecodeScratch& ws, int32_t* err,
+                                        cudaStream_t s);
 
 // QKV projection of listed rows: q / k / v rows of token t_i = tokens[i] (null: i) from
 // x[x_index[i]] W^T (x_index null: x[i], read in place; else the rows are first copied to

@@ -56,3 +56,39 @@ def test_attention_wait_timeout_is_reported_and_the_device_stays_usable(cb):
         cb.cb_test_attention_wait_timeout(plan, dq, pos, mq, dk, dv, 128, out)  # no key tile 1 to miss
     assert e.value.status == 1
     plan.close()
+
+
+def test_decode_wait_timeout_is_reported_and_the_plan_stays_usable(cb):
+    # cb_test_decode_wait_timeout: the decode kernel whose producer never copies key tile 1 of its
+    # split and whose waits give up after 100 us. Every CTA with a second tile records the timeout,
+    # drains, frees its tensor memory and still takes its ticket; a normal decode on the same plan
+    # right after (same split counters) must then match the oracle.
+    from oracle.attention import decode_attention
+
+    hq, hkv, d, n_keys = 32, 8, 128, 3137
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1, chunk_len=n_keys - 1,
+                              n_suffix=1)
+    plan = cb.Plan.from_config(cfg)
+    rng = np.random.default_rng(405)
+    q = f32_to_bf16_bits(rng.standard_normal((hq, d)).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    dq, dk, dv = bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+    out = torch.zeros((hq, d), dtype=torch.bfloat16, device="cuda")
+    ref = decode_attention(bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    for _ in range(2):  # the failure and the recovery, twice in a row
+        t0 = time.perf_counter()
+        cb.cb_test_decode_wait_timeout(plan, dq, dk, dv, n_keys, out)
+        with pytest.raises(cb.CacheBlendError) as e:
+            plan.check()
+        assert e.value.status == 4 and "flags 0x8 " in str(e.value)
+        assert time.perf_counter() - t0 < 30.0
+        plan.check()
+        out.zero_()
+        cb.cb_decode_attention(plan, dq, dk, dv, n_keys, out)
+        plan.check()
+        assert_close_bf16(bf16_bits_to_f64(bf16_bits(out)), ref, what="decode after a timed-out launch")
+    with pytest.raises(cb.CacheBlendError) as e:
+        cb.cb_test_decode_wait_timeout(plan, dq, dk, dv, 128, out)  # no key tile 1 to miss
+    assert e.value.status == 1
+    plan.close()
