@@ -382,6 +382,19 @@ cb_status cb_test_attention_wait_timeout(cb_plan* plan, const void* q, const int
 cb_status cb_test_decode_wait_timeout(cb_plan* plan, const void* q, const void* k, const void* v, int32_t n_keys,
                                       void* out, void* stream);
 
+/* Test support for the failure path, not part of the blend (the pages have no
+ * counterpart). Runs cb_qkv_projection's kernel (head_dim 128; x[0 .. m) read in
+ * place, written at tokens 0 .. m-1, no RoPE) in a form where the first CTA of
+ * every CTA pair arms the barrier of K step 1 for the pair's bytes but never
+ * copies its own share, and every bounded wait gives up after 100 us instead of
+ * 2 s: both CTAs record CB_ERR_TIMEOUT in the plan's error word, drain the MMAs
+ * and copies they started, free their tensor memory and meet at the final
+ * cluster barrier; q, k, v are left unwritten or partly written. The next
+ * cb_check reports CB_ERR_TIMEOUT and clears the word, and the device stays
+ * usable. CB_ERR_INVALID_ARG unless 0 < m <= n_tokens and d_model >= 128. */
+cb_status cb_test_projection_wait_timeout(cb_plan* plan, const void* x, int32_t d_model, int32_t m,
+                                          const void* w_qkv, void* q, void* k, void* v, void* stream);
+
 /* Synchronise the plan's device, read and clear its error word. Returns
  * CB_OK, CB_ERR_TIMEOUT or CB_ERR_DEVICE_CHECK (detail in
  * cb_last_error_string). Off the hot path. */

@@ -19,7 +19,8 @@ __all__ = ["Plan", "CacheBlendError", "cb_rope_rerotate", "cb_kv_deviation", "cb
            "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention", "cb_attention_sparsity",
            "cb_output_deviation", "cb_qkv_projection", "cb_qkv_projection_indexed", "cb_blend_layer", "cb_blend_stage",
            "cb_blend_request", "cb_hkvd_select_noalloc", "cb_attention_uses_paired_tiles",
-           "cb_test_attention_wait_timeout", "cb_test_decode_wait_timeout", "cb_check", "cb_version",
+           "cb_test_attention_wait_timeout", "cb_test_decode_wait_timeout", "cb_test_projection_wait_timeout",
+           "cb_check", "cb_version",
            "LayerBuffers"]
 
 
@@ -218,6 +219,13 @@ def cb_test_decode_wait_timeout(plan, q, k, v, n_keys, out, stream=None):
     check(_lib.load().cb_test_decode_wait_timeout(
         plan.handle, _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
         n_keys, _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def cb_test_projection_wait_timeout(plan, x, m, w_qkv, q, k, v, stream=None):
+    """The QKV projection in a form whose bounded waits run out (see cacheblend.h; test support)."""
+    check(_lib.load().cb_test_projection_wait_timeout(
+        plan.handle, _ptr(x, torch.bfloat16, "x"), x.shape[1], m, _ptr(w_qkv, torch.bfloat16, "w_qkv"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"), _stream(stream)))
 
 
 def cb_test_attention_wait_timeout(plan, q, q_pos, mq, k, v, n_keys, out, stream=None):

@@ -27,7 +27,8 @@ EXPORTS = ("cb_plan_create", "cb_plan_destroy", "cb_layer_sizes", "cb_rope_rerot
            "cb_kv_deviation_kv", "cb_hkvd_topk", "cb_fuse_scatter", "cb_hkvd_attention", "cb_decode_attention",
            "cb_attention_sparsity", "cb_output_deviation", "cb_qkv_projection", "cb_qkv_projection_indexed",
            "cb_blend_layer", "cb_blend_stage", "cb_blend_request", "cb_hkvd_select_noalloc",
-           "cb_attention_uses_paired_tiles", "cb_test_attention_wait_timeout", "cb_test_decode_wait_timeout", "cb_check",
+           "cb_attention_uses_paired_tiles", "cb_test_attention_wait_timeout", "cb_test_decode_wait_timeout",
+           "cb_test_projection_wait_timeout", "cb_check",
            "cb_last_error_string", "cb_version")
 
 
@@ -86,6 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cb_attention_uses_paired_tiles": (i32, [vp, i32]),
         "cb_test_attention_wait_timeout": (i32, [vp, vp, vp, i32, vp, vp, i32, vp, vp]),
         "cb_test_decode_wait_timeout": (i32, [vp, vp, vp, vp, i32, vp, vp]),
+        "cb_test_projection_wait_timeout": (i32, [vp, vp, i32, i32, vp, vp, vp, vp, vp]),
         "cb_check": (i32, [vp]),
         "cb_last_error_string": (ctypes.c_char_p, []),
         "cb_version": (i32, []),

@@ -373,6 +373,25 @@ cb_status cb_test_decode_wait_timeout(cb_plan* plan, const void* q, const void* 
                      "cb_test_decode_wait_timeout");
 }
 
+cb_status cb_test_projection_wait_timeout(cb_plan* plan, const void* x, int32_t d_model, int32_t m,
+                                          const void* w_qkv, void* q, void* k, void* v, void* stream) {
+  CB_NVTX_RANGE();
+  CB_TRY(check_plan(plan));
+  if (plan->cfg.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "the wait-timeout probe needs head_dim 128");
+  if (m <= 0 || m > plan->n_tokens) return fail(CB_ERR_INVALID_ARG, "the wait-timeout probe needs 0 < m <= n_tokens");
+  if (d_model < 128 || d_model % 64 != 0)
+    return fail(CB_ERR_INVALID_ARG, "the wait-timeout probe needs d_model >= 128, a multiple of 64");
+  CB_TRY(need_tensor(x, "x"));
+  CB_TRY(need_tensor(w_qkv, "w_qkv"));
+  CB_TRY(need_tensor(q, "q"));
+  CB_TRY(need_tensor(k, "k"));
+  CB_TRY(need_tensor(v, "v"));
+  const auto& c = plan->cfg;
+  return cuda_status(cb::launch_projection_timeout_probe(x, d_model, m, w_qkv, plan->n_tokens, c.hq, c.hkv, q, k, v,
+                                                         plan->err, static_cast<cudaStream_t>(stream)),
+                     "cb_test_projection_wait_timeout");
+}
+
 cb_status cb_attention_sparsity(cb_plan* plan, const void* q, const int32_t* q_pos, int32_t mq, const void* k,
                                 const void* v, int32_t n_keys, float scale, float eps, void* out, void* row_stats,
                                 int32_t* counts, uint64_t* total, void* stream) {

@@ -159,5 +159,10 @@ cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model
                                   int32_t hq, int32_t hkv, int32_t head_dim, int32_t encode, int32_t style, RopeTable t,
                                   void* q, void* k, void* v, int32_t* err, cudaStream_t s);
 bool qkv_projection_supported(int32_t d_model);
+// Test support: the projection kernel (head_dim 128, x read in place, no RoPE) in a form whose K
+// step 1 never completes and whose waits give up after kProbeTimeoutNs (d_model >= 128).
+cudaError_t launch_projection_timeout_probe(const void* x, int32_t d_model, int32_t m, const void* w, int32_t n_tokens,
+                                            int32_t hq, int32_t hkv, void* q, void* k, void* v, int32_t* err,
+                                            cudaStream_t s);
 
 }  // namespace cb

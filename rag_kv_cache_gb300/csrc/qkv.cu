@@ -119,9 +119,10 @@ __device__ __forceinline__ void pair_bar_sync(int id) { asm volatile("bar.sync %
 // gave up in one warp cannot leave its partner at a pair barrier.
 template <int D>
 __device__ __forceinline__ void proj_epilogue(const ProjParams& p, uint32_t acc_bar, uint32_t tmem, uint32_t sA0,
-                                              const int* s_rows, int m0, int n0, volatile int* abort_flag) {
+                                              const int* s_rows, int m0, int n0, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const bool acc_ok = mbar_wait(acc_bar, 0, abort_flag, p.err, 44);
+  const bool acc_ok = mbar_wait(acc_bar, 0, abort_flag, p.err, 44, true, limit_ns);
   if (__syncthreads_and(acc_ok ? 1 : 0)) {
     tc_fence_after();
     const int g = warp & 3, upper = warp >> 2;
@@ -285,7 +286,11 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       : "memory");
 }
 
-template <int D>
+// PROBE: the wait-timeout probe (test support only): CTA 0 arms the barrier of K step 1 for the
+// pair's bytes but never copies its own share, and every wait gives up after kProbeTimeoutNs, so
+// both CTAs of every pair take the failure path (timeout recorded, the MMAs issued so far drained,
+// TMEM freed, both at the final cluster barrier).
+template <int D, bool PROBE = false>
 __global__ void __launch_bounds__(kPThreads, 1)
     qkv_projection_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                const ProjParams p) {
@@ -305,6 +310,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int n0 = blockIdx.y * kPN;          // the pair's 256 output features
   const int nb = n0 + (int)rank * (kPN / 2);  // this CTA's half of the W slice
   const int n_k = p.d_model / kPK;
+  constexpr uint64_t kLimit = PROBE ? kProbeTimeoutNs : kTimeoutNs;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
@@ -346,19 +352,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int kk = 0; kk < n_k; ++kk) {
         const int st = kk % kQStages;
         if (kk >= kQStages &&
-            !mbar_spin(smem_u32(&bars.empty[st]), ((kk / kQStages) - 1) & 1, abort_flag, p.err, 50))
+            !mbar_spin(smem_u32(&bars.empty[st]), ((kk / kQStages) - 1) & 1, abort_flag, p.err, 50, kLimit))
           break;
         if (rank == 0) mbar_expect_tx(smem_u32(&bars.full[st]), 4 * kQHalfBytes);  // both CTAs' bytes
         const uint32_t fb = full0 + (uint32_t)st * 8u;
+        issued = kk + 1;
+        if (PROBE && rank == 0 && kk == 1) continue;  // the probe's stage that can never complete
         tma_load_2d_pair(sA0 + st * kQHalfBytes, &tm_x, fb, kk * kPK, m0);  // rows past m read as zeros
         tma_load_2d_pair(sB0 + st * kQHalfBytes, &tm_w, fb, kk * kPK, nb);
-        issued = kk + 1;
       }
       // CTA 0: every copy of the pair that was issued has landed (CTA 1 waits for CTA 0 at the
       // final cluster barrier, so it cannot exit with copies in flight either)
       if (rank == 0)
         for (int kk = issued - kQStages < 0 ? 0 : issued - kQStages; kk < issued; ++kk)
-          mbar_wait(smem_u32(&bars.full[kk % kQStages]), (kk / kQStages) & 1, abort_flag, p.err, 51, false);
+          mbar_wait(smem_u32(&bars.full[kk % kQStages]), (kk / kQStages) & 1, abort_flag, p.err, 51, false, kLimit);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int kk = 0; kk < n_k && ok; ++kk) {
         const int st = kk % kQStages;
         const uint32_t par = (kk / kQStages) & 1;
-        ok = __all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.full[st]), par, abort_flag, p.err, 52));
+        ok = __all_sync(0xffffffffu, mbar_spin(smem_u32(&bars.full[st]), par, abort_flag, p.err, 52, kLimit));
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
     }
     // neither CTA frees TMEM or exits while the pair's MMAs may still read or write it
-    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 54, false);
+    mbar_wait(smem_u32(&bars.drain), 0, abort_flag, p.err, 54, false, kLimit);
   } else if (warp >= 4) {
     // token of each of this CTA's rows (-1: past m, or outside the cache: not stored); only the
     // epilogue reads them, after its CTA-wide barrier
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     s_rows[threadIdx.x - 128] = t;
   }
 
-  proj_epilogue<D>(p, smem_u32(&bars.acc_full), tmem, sA0, s_rows, m0, n0, abort_flag);
+  proj_epilogue<D>(p, smem_u32(&bars.acc_full), tmem, sA0, s_rows, m0, n0, abort_flag, kLimit);
 
   tc_fence_before();
   cluster_sync_all();  // neither CTA exits while the other may still arrive on its barriers
@@ -436,7 +443,7 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool PROBE = false>
 cudaError_t launch_proj_pair(const ProjParams& p, const void* x, const void* w, cudaStream_t s) {
   const int n_out = (p.hq + 2 * p.hkv) * D;
   CUtensorMap tx, tw;
@@ -445,7 +452,7 @@ cudaError_t launch_proj_pair(const ProjParams& p, const void* x, const void* w, 
     return cudaErrorInvalidValue;
   const size_t smem = 1024 + (size_t)kQStages * 2 * kQHalfBytes;
   static std::atomic<uint64_t> configured{0};
-  const cudaError_t e = set_smem_limit_once(qkv_projection_pair_kernel<D>, (int)smem, configured);
+  const cudaError_t e = set_smem_limit_once(qkv_projection_pair_kernel<D, PROBE>, (int)smem, configured);
   if (e != cudaSuccess) return e;
   const int m_tiles = (p.m + kPM - 1) / kPM;
   const dim3 grid((unsigned)(2 * ((m_tiles + 1) / 2)), (n_out + kPN - 1) / kPN);  // whole pairs
@@ -463,7 +470,7 @@ cudaError_t launch_proj_pair(const ProjParams& p, const void* x, const void* w, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qkv_projection_pair_kernel<D>, tx, tw, p);
+  return cudaLaunchKernelEx(&cfg, qkv_projection_pair_kernel<D, PROBE>, tx, tw, p);
 }
 
 }  // namespace
@@ -502,5 +509,23 @@ cudaError_t launch_qkv_projection(const void* x, int32_t x_rows, int32_t d_model
 }
 
 bool qkv_projection_supported(int32_t d_model) { return d_model >= kPK && d_model % kPK == 0; }
+
+cudaError_t launch_projection_timeout_probe(const void* x, int32_t d_model, int32_t m, const void* w, int32_t n_tokens,
+                                            int32_t hq, int32_t hkv, void* q, void* k, void* v, int32_t* err,
+                                            cudaStream_t s) {
+  if (m <= 0 || d_model < 2 * kPK || d_model % kPK != 0) return cudaErrorInvalidValue;  // needs a K step 1
+  ProjParams p = {};
+  p.m = m;
+  p.n_tokens = n_tokens;
+  p.d_model = d_model;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.head_dim = 128;
+  p.q = static_cast<uint8_t*>(q);
+  p.k = static_cast<uint8_t*>(k);
+  p.v = static_cast<uint8_t*>(v);
+  p.err = err;
+  return launch_proj_pair<128, true>(p, x, w, s);
+}
 
 }  // namespace cb

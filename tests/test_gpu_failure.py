@@ -92,3 +92,41 @@ def test_decode_wait_timeout_is_reported_and_the_plan_stays_usable(cb):
         cb.cb_test_decode_wait_timeout(plan, dq, dk, dv, 128, out)  # no key tile 1 to miss
     assert e.value.status == 1
     plan.close()
+
+
+def test_projection_wait_timeout_is_reported_and_the_device_stays_usable(cb):
+    # cb_test_projection_wait_timeout: the CTA-pair projection kernel whose first CTA of each pair
+    # never copies its share of K step 1 (the pair's barrier for it cannot complete) and whose
+    # waits give up after 100 us. Both CTAs of every pair must record the timeout, drain, free
+    # their tensor memory and meet at the cluster barrier; a normal projection right after must
+    # match the oracle.
+    from oracle.projection import qkv_projection
+    from workloads.generator import generate_projection
+
+    cfg = dataclasses.replace(get_config("tiny"), hq=8, hkv=2, head_dim=128, d_model=512, n_chunks=1, chunk_len=392,
+                              n_suffix=8)
+    plan = cb.Plan.from_config(cfg)
+    m = 300  # three row tiles: two CTA pairs, one of them half past m
+    x, w = generate_projection(cfg, 3)
+    dx, dw = bf16_tensor(x[:m]), bf16_tensor(w)
+    shape = lambda h: (cfg.n_tokens, h, cfg.head_dim)
+    q, k, v = (torch.zeros(shape(h), dtype=torch.bfloat16, device="cuda") for h in (cfg.hq, cfg.hkv, cfg.hkv))
+    oq, ok, ov = qkv_projection(bf16_bits_to_f64(x), np.arange(m), bf16_bits_to_f64(w), cfg.hq, cfg.hkv,
+                                cfg.head_dim, cfg.rope_theta, False)
+    for _ in range(2):  # the failure and the recovery, twice in a row
+        t0 = time.perf_counter()
+        cb.cb_test_projection_wait_timeout(plan, dx, m, dw, q, k, v)
+        with pytest.raises(cb.CacheBlendError) as e:
+            plan.check()
+        assert e.value.status == 4 and "flags 0x8 " in str(e.value)
+        assert time.perf_counter() - t0 < 30.0
+        plan.check()
+        cb.cb_qkv_projection_indexed(plan, dx, None, None, m, dw, q, k, v)
+        plan.check()
+        for got, want, what in ((q, oq, "q"), (k, ok, "k"), (v, ov, "v")):
+            assert_close_bf16(bf16_bits_to_f64(bf16_bits(got[:m])), want, what=f"projection {what} after a timeout")
+    with pytest.raises(cb.CacheBlendError) as e:
+        cb.cb_test_projection_wait_timeout(plan, bf16_tensor(x[:m, :64].copy()), m, bf16_tensor(w[:, :64].copy()),
+                                           q, k, v)  # d_model 64: no K step 1 to miss
+    assert e.value.status == 1
+    plan.close()
