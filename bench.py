@@ -822,7 +822,8 @@ def run_decode(args, cfg):
                        "l2": f"inputs larger than L2: {cfg.layers * bytes_launch / 1e9:.2f} GB per step",
                        "cuda_graph": True},
             "roofline": {"kernel": "decode_tc", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": (traffic_for("decode_tc.cu", cfg.name) or {}).get("dram_bytes_per_launch"),
                          "peak_source": f"{peaks['source']} copy bandwidth", "bytes_per_launch": bytes_launch,
                          "launches_per_step": cfg.layers, "avg_launch_us": us_launch},
             "gpu_launches": cfg.layers * args.steps, "clocks": clocks.summary()}
@@ -1052,7 +1053,8 @@ def run_projection(args, cfg):
                                "attention rows, in list order); layer 1 all tokens",
                        "l2": "four weight sets cycled (4 x %.0f MB)" % (n_out * d_model * 2 / 1e6)},
             "roofline": {"kernel": "qkv_projection_pair", "bound": "tensor", "achieved": tf, "peak": peak,
-                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": tf / peak,
+                         "traffic": (traffic_for("qkv.cu", cfg.name) or {}).get("dram_bytes_per_launch"),
                          "peak_source": f"{peaks['source']} bf16 sustained", "flops_per_step": flops},
             "gathered_rows": {"ms_per_step": ms_gathered, "achieved": tf_g, "frac": tf_g / peak,
                               "how": "every layer's rows gathered from a full [n_tokens, d_model] matrix first "
