@@ -5,18 +5,19 @@
 //
 // On the CUDA cores one key of one kv head costs about 2,000 flops of dot products, shuffle
 // reductions and P V sums at G = 4-8, which an earlier form of this kernel found near the issue
-// limit instead of the HBM limit (Llama-70B shape 23 us per layer, 0.22 of HBM). Here the G query heads of a kv head are rows 0 .. G-1 of a 128-row Q tile and
-// each key tile takes the attention kernel's path: S = Q K_j^T (tcgen05, M 128, N 128 keys,
-// K = D), one thread per head row turns S into P = 2^(s - m) in TMEM, and O += P V_j (P from
-// TMEM, V MN-major). The tensor core does 16x the needed rows, which still leaves it idle most
-// of the time: a 128-key tile is 64 KiB of K and V, about 2,850 cycles of an SM's share of HBM,
-// against ~2,000 cycles of MMAs.
+// limit instead of the HBM limit (Llama-70B shape 23 us per layer, 0.22 of HBM). Here the G query
+// heads of a kv head are rows 0 .. G-1 of a 128-row Q tile and each key tile takes the attention
+// kernel's path: S = Q K_j^T (tcgen05, M 128, N 128 keys, K = D), one thread per head row turns S
+// into P = 2^(s - m) in TMEM, and O += P V_j (P from TMEM, V MN-major). The tensor core does 16x
+// the needed rows, which still leaves it idle most of the time: a 128-key tile is 64 KiB of K and
+// V, about 2,850 cycles of an SM's share of HBM, against ~2,000 cycles of MMAs.
 //
 // Grid (splits, Hkv), one CTA per SM, splits x Hkv at most one wave: a CTA takes a contiguous
-// range of key tiles of one kv head. Warp 0 streams K and V tiles through two 3-stage rings
-// (TMA, 128-byte swizzle), warp 1 issues the MMAs (S double-buffered in TMEM, so S_{j+1} is
-// computed while the softmax works on tile j), warp 4 (TMEM lanes 0-31) runs the online softmax
-// with one thread per head row (rows G .. 31 are inactive). Each CTA leaves (max, sum,
+// range of key tiles of one kv head, and its first tiles are prefetched into L2 before it waits
+// for the kernels it depends on. Warp 0 streams K and V tiles through two 3-stage rings (TMA,
+// 128-byte swizzle), warp 1 issues the MMAs (S double-buffered in TMEM, so S_{j+1} is computed
+// while the softmax works on tile j), warp 4 (TMEM lanes 0-31) runs the online softmax with one
+// thread per head row (rows G .. 31 are inactive). Each CTA leaves (max, sum,
 // unnormalised O rows) in the plan's decode scratch and the last CTA of a kv head (a ticket
 // counter) merges the splits. Every mbarrier wait is bounded (2 s): a wait that gives up
 // records a timeout, the CTA drains its copies and MMAs, frees TMEM and returns.
