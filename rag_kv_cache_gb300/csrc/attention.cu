@@ -81,6 +81,7 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int b, int h) { return (uint32_t)(b * kBN + h * kHalf); }
 __host__ __device__ constexpr uint32_t col_o(int h, int d) { return 256u + (uint32_t)(h * d); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kTileSumLimit = 65536.0f;  // a later tile whose P sum exceeds 2^16 moves the reference
 
 // One MMA commit per product: S_j's completion frees K stage j % 3 and tells the softmax that S_j
 // is in TMEM (both wait on s_done[j % 3], phase j / 3); P V_j's completion frees V stage j % 3 and
@@ -127,8 +128,31 @@ struct Params {
 // PROBE: the wait-timeout probe (test support only): the K producer never requests key tile 1
 // and every wait gives up after kProbeTimeoutNs, so the CTA takes its failure path (timeout
 // recorded, remaining rounds skipped, copies and tensor-core work drained, TMEM freed).
+// One row's P for its half of a key tile: P = 2^(s * scale - m_ref) for its 64 scores (m_ref = -inf
+// only for a row with nothing visible yet, whose scores are then all -inf), packed to bf16 into pk
+// (key 2e in the low half of pk[e]); returns the row sum of P (fp32, +inf if an exponent overflowed).
+__device__ __forceinline__ float softmax_p(const uint32_t (&sv)[kHalf], float m_ref, float scale_log2,
+                                           uint32_t (&pk)[kHalf / 2]) {
+  const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
+  uint64_t ps2[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
+#pragma unroll
+  for (int e = 0; e < kHalf / 2; ++e) {
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2, nm2), t0, t1);
+    const float p0 = ex2(t0), p1 = ex2(t1);
+    ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
+    pk[e] = pack2(p0, p1);
+  }
+  float sa, sb;
+  f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa, sb);
+  return sa + sb;
+}
+
 template <int D, bool COUNT, bool PROBE = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(128)
     hkvd_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           const Params p) {
@@ -419,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld(sb);
       }
       const int lim = my_pos - (j * kBN + wg * kHalf);  // columns c <= lim are visible to this row
-      if (__any_sync(0xffffffffu, lim < kHalf - 1)) {  // diagonal tiles only
+      const bool diag = __any_sync(0xffffffffu, lim < kHalf - 1);  // diagonal tiles only
+      if (diag) {
 #pragma unroll
         for (int c = 0; c < kHalf; ++c)
           if (c > lim) sv[c] = 0xff800000u;  // -inf
@@ -429,65 +454,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kHalf; ++c) cnt += __uint_as_float(sv[c]) * p.scale_log2 < tau ? 1 : 0;
       }
 
-      // Row max of this half tile from the registers, before any exponential: the reference m_ref
-      // (log2 units) that O and l are scaled to moves up only when a tile's max passes it by more
-      // than 2^8, so every exponent below is at most kRescaleThreshold and O is rescaled rarely.
-      // Four independent chains of three-input max (8 deep each).
-      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < kHalf; c += 8) {
-        tm[0] = max3(tm[0], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-        tm[1] = max3(tm[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-        tm[2] = max3(tm[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
-        tm[3] = max3(tm[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
-      }
-      const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
-      const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
-      if (__any_sync(0xffffffffu, up)) {
-        // alpha = 2^(m_ref - mt): 0 for a row that had nothing visible (its O and l are zero).
-        const float alpha = up ? ex2(m_ref - mt) : 1.0f;
-        const bool scale_o = up && m_ref != -INFINITY;
-        if (up) {
-          l *= alpha;
-          m_ref = mt;
-        }
-        // O holds this warpgroup's sum through tile j - 1: wait for that P V, then scale it.
-        if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
-          if (!wait_pv(j - 1, 22 + wg)) return false;
-          tc_fence_after();
-          const float a = scale_o ? alpha : 1.0f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(lane_base + col_o(wg, D) + c0, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-            tmem_st_x32(lane_base + col_o(wg, D) + c0, o);
-          }
-          tmem_st_wait();
-        }
-      }
-      // P = 2^(s * scale - m_ref) <= 2^8, packed to bf16, and its row sum. A row with nothing visible
-      // yet has only -inf scores, so P = 0 (the offset 0 stands in for its missing reference).
+      // P = 2^(s * scale - m_ref), packed to bf16, and its row sum. A row's first visible tile sets
+      // the reference m_ref (log2 units) that O and l are scaled to: the max of its scores. Later
+      // tiles run the exponentials against the reference without taking their max first (the
+      // softmax is on the tile loop's critical path): a half tile whose row sum stays within 2^16
+      // has every P within 2^16, far from overflow in P, O and l. One whose sum passes that (its
+      // max grew by more than 2^10) takes its max, moves the reference of the rows whose max passes
+      // it by more than 2^8, rescales O and computes P again (from the scores loaded again: S is
+      // still in TMEM, since P is stored over it only at the end, and the registers are not kept).
+      // A row with nothing visible yet has only -inf scores, so P = 0 (the offset 0 stands in for
+      // its missing reference).
       uint32_t pk[kHalf / 2];
-      {
-        const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
-        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
-        uint64_t ps2[4];
+      bool move_ref = !__all_sync(0xffffffffu, m_ref != -INFINITY);
+      float sum = 0.0f;
+      if (!move_ref) {
+        sum = softmax_p(sv, m_ref, p.scale_log2, pk);
+        if (!__all_sync(0xffffffffu, sum <= kTileSumLimit)) {  // rare: the max jumped
+          move_ref = true;
+          uint32_t(&sa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+          uint32_t(&sb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+          tmem_ld_x32_async(lane_base + col_s(b, wg), sa);
+          tmem_ld_x32_async(lane_base + col_s(b, wg) + 32, sb);
+          tmem_wait_ld(sa);
+          tmem_wait_ld(sb);
+          if (diag) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
-#pragma unroll
-        for (int e = 0; e < kHalf / 2; ++e) {
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2, nm2), t0, t1);
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
-          pk[e] = pack2(p0, p1);
+            for (int c = 0; c < kHalf; ++c)
+              if (c > lim) sv[c] = 0xff800000u;  // -inf
+          }
         }
-        float sa_, sb_;
-        f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa_, sb_);
-        l += sa_ + sb_;
       }
+      if (move_ref) {
+        // Four independent chains of three-input max (8 deep each).
+        float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 8) {
+          tm[0] = max3(tm[0], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+          tm[1] = max3(tm[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+          tm[2] = max3(tm[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+          tm[3] = max3(tm[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+        }
+        const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
+        const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
+        if (__any_sync(0xffffffffu, up)) {
+          // alpha = 2^(m_ref - mt): 0 for a row that had nothing visible (its O and l are zero).
+          const float alpha = up ? ex2(m_ref - mt) : 1.0f;
+          const bool scale_o = up && m_ref != -INFINITY;
+          if (up) {
+            l *= alpha;
+            m_ref = mt;
+          }
+          // O holds this warpgroup's sum through tile j - 1: wait for that P V, then scale it.
+          if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
+            if (!wait_pv(j - 1, 22 + wg)) return false;
+            tc_fence_after();
+            const float a = scale_o ? alpha : 1.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(lane_base + col_o(wg, D) + c0, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+              tmem_st_x32(lane_base + col_o(wg, D) + c0, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        sum = softmax_p(sv, m_ref, p.scale_log2, pk);
+      }
+      l += sum;
       tmem_st_x32(lane_base + col_s(b, wg), pk);
       tmem_st_wait();
       return true;

@@ -76,6 +76,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxRegs = 224;  // per thread of WG0 / WG1 after setmaxnreg.inc
 constexpr int kOtherRegs = 56;     // per thread of WG2 after setmaxnreg.dec
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kTileSumLimit = 65536.0f;  // a later tile whose P sum exceeds 2^16 moves the reference
 
 __host__ __device__ constexpr uint32_t col_s(int i) { return (uint32_t)(i * kBN); }
 __host__ __device__ constexpr uint32_t col_o(int i, int d) { return 256u + (uint32_t)(i * d); }
@@ -107,6 +108,36 @@ struct PPParams {
 
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// One row's P for a key tile: P = 2^(s * scale - m_ref) for its 128 scores (m_ref = -inf only for
+// a row with nothing visible yet, whose scores are then all -inf), packed to bf16 and written to
+// TMEM as 32 columns per 64 keys from taddr_p; returns the row sum of P (fp32, +inf if an exponent
+// overflowed).
+__device__ __forceinline__ float softmax_p(const uint32_t (&sv)[kBN], float m_ref, float scale_log2,
+                                           uint32_t taddr_p) {
+  const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
+  uint64_t ps2[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = 64 * h + 2 * e;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nm2), x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
+      pk[e] = pack2(p0, p1);
+    }
+    tmem_st_x32(taddr_p + 32 * h, pk);
+  }
+  float sa, sb;
+  f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa, sb);
+  return sa + sb;
 }
 
 template <int D>
@@ -380,66 +411,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (c > lim) sv[c] = 0xff800000u;  // -inf
       }
-      // Row max of the tile before any exponential; the reference m_ref moves up only when the
-      // tile's max passes it by more than 2^8, so every exponent below is at most 8 and O is
-      // rescaled rarely. Four independent chains of three-input max.
-      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
-        tm[0] = max3(tm[0], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-        tm[1] = max3(tm[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-        tm[2] = max3(tm[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
-        tm[3] = max3(tm[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+      // P = 2^(s * scale - m_ref), packed to bf16 and written over the first half of S_ti (32
+      // columns per 64 keys), and its row sum. A row's first visible tile sets the reference m_ref
+      // to the tile's max. Later tiles run the exponentials against the reference without taking
+      // their max first (the softmax sets the round's pace): a tile whose row sum stays within
+      // 2^16 has every P within 2^16, far from overflow in P, O and l. A tile whose sum passes
+      // that (its max grew by more than 2^9) takes its max, moves the reference of the rows whose
+      // max passes it by more than 2^8, rescales O and computes P again before the issuer reads it.
+      const uint32_t taddr_p = lane_base + col_s(ti);
+      bool move_ref = !__all_sync(0xffffffffu, m_ref != -INFINITY);  // a row's first visible tile
+      float sum = 0.0f;
+      if (!move_ref) {
+        sum = softmax_p(sv, m_ref, p.scale_log2, taddr_p);
+        move_ref = !__all_sync(0xffffffffu, sum <= kTileSumLimit);  // rare: the max jumped
       }
-      const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
-      const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
-      if (__any_sync(0xffffffffu, up)) {
-        const float alpha = up ? ex2(m_ref - mt) : 1.0f;  // 0 for a row that had nothing visible
-        const bool scale_o = up && m_ref != -INFINITY;
-        if (up) {
-          l *= alpha;
-          m_ref = mt;
-        }
-        // O_ti holds the sum through tile j - 1: wait for that product, then scale it.
-        if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
-          if (!wait_o(j - 1, 22 + ti)) return false;
-          tc_fence_after();
-          const float a = scale_o ? alpha : 1.0f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(lane_base + col_o(ti, D) + c0, o);
+      if (move_ref) {
+        // Four independent chains of three-input max.
+        float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
-            tmem_st_x32(lane_base + col_o(ti, D) + c0, o);
+        for (int c = 0; c < kBN; c += 8) {
+          tm[0] = max3(tm[0], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+          tm[1] = max3(tm[1], __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+          tm[2] = max3(tm[2], __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+          tm[3] = max3(tm[3], __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+        }
+        const float mt = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * p.scale_log2;  // -inf: nothing visible
+        const bool up = mt > m_ref + kRescaleThreshold;  // always, at a row's first visible key
+        if (__any_sync(0xffffffffu, up)) {
+          const float alpha = up ? ex2(m_ref - mt) : 1.0f;  // 0 for a row that had nothing visible
+          const bool scale_o = up && m_ref != -INFINITY;
+          if (up) {
+            l *= alpha;
+            m_ref = mt;
           }
-          tmem_st_wait();
+          // O_ti holds the sum through tile j - 1: wait for that product, then scale it.
+          if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
+            if (!wait_o(j - 1, 22 + ti)) return false;
+            tc_fence_after();
+            const float a = scale_o ? alpha : 1.0f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(lane_base + col_o(ti, D) + c0, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+              tmem_st_x32(lane_base + col_o(ti, D) + c0, o);
+            }
+            tmem_st_wait();
+          }
         }
+        sum = softmax_p(sv, m_ref, p.scale_log2, taddr_p);  // these stores replace any earlier P
       }
-      // P = 2^(s * scale - m_ref) <= 2^8, packed to bf16, and its row sum; each half of the tile
-      // (64 keys) is written as 32 columns over the first half of S_ti.
-      const float neg_m = m_ref == -INFINITY ? 0.0f : -m_ref;
-      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(neg_m, neg_m);
-      uint64_t ps2[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) ps2[q] = f2_pack(0.0f, 0.0f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = 64 * h + 2 * e;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ps2[e & 3] = f2_add(ps2[e & 3], f2_pack(p0, p1));
-          pk[e] = pack2(p0, p1);
-        }
-        tmem_st_x32(lane_base + col_s(ti) + 32 * h, pk);
-      }
-      float sa_, sb_;
-      f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sa_, sb_);
-      l += sa_ + sb_;
+      l += sum;
       tmem_st_wait();
       return true;
     };

@@ -422,6 +422,40 @@ def test_paired_tile_attention_sparse_rows(cb, hq, hkv, mq, n_keys):
     assert_close_bf16(got, ref, what=f"paired-tile attention hq={hq} hkv={hkv} mq={mq}")
 
 
+def test_paired_tile_attention_score_jumps(cb):
+    # The paired-tile kernel runs a row's later key tiles against its running reference and
+    # takes the tile max only when the tile's P sum passes its limit. Keys whose scores exceed
+    # everything before them by far more than 2^64 (base-2 units of the scaled score), in the
+    # first and second half of odd and even key tiles, make that sum overflow: the tile must be
+    # redone against a moved reference, with O rescaled.
+    hq, hkv, d, n_keys, mq = 32, 8, 128, 4000, 2500
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=n_keys - 1, n_suffix=1)
+    plan = _plan(cb, cfg)
+    assert cb.cb_attention_uses_paired_tiles(plan, mq)
+    rng = np.random.default_rng(33)
+    q_pos = np.sort(rng.choice(n_keys, size=mq, replace=False))
+    q = f32_to_bf16_bits((1.0 + 0.1 * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    kf = rng.standard_normal((n_keys, hkv, d)).astype(np.float32)
+    kf[300] = 6.0    # tile 2, second half
+    kf[1410] = 8.0   # tile 11, first half
+    kf[2705] = 12.0  # tile 21, second half
+    kf[3350] = 12.5  # tile 26, first half
+    k = f32_to_bf16_bits(kf)
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    got = bf16_bits_to_f64(bf16_bits(out))
+    assert np.all(np.isfinite(got))
+    # rows on both sides of every spike, plus seeded rows
+    near = [np.searchsorted(q_pos, t) + o for t in (300, 1410, 2705, 3350) for o in (-1, 0, 1)]
+    pick = np.unique(np.clip(np.concatenate([near, [0, mq - 1], rng.choice(mq, size=160, replace=False)]), 0, mq - 1))
+    ref = causal_gqa_attention(bf16_bits_to_f64(q[pick]), q_pos[pick], bf16_bits_to_f64(k), bf16_bits_to_f64(v))
+    plan.close()
+    assert_close_bf16(got[pick], ref, what="paired-tile attention with score jumps")
+
+
 def test_paired_tile_attention_dense_suffix_and_rescale(cb):
     # every position from 0 (causal diagonal in every key tile), keys that force the running max
     # up by more than 2^8 inside the loop
