@@ -838,9 +838,11 @@ def run_decode(args, cfg):
 def run_diagnostics(args, cfg):
     """Diagnostics path on one layer: for every recompute ratio of the workload's sweep (else r1),
     blend the layer and measure ||Attn(Q, K_fused, V_fused) - Attn(Q, K_new, V_new)|| over all
-    query rows against a full prefill, and the full prefill's Sparsity(A, eps). Times the
-    diagnostics of one ratio: both encodes, the fused-cache attention, the two passes of the
-    sparsity count and the reductions."""
+    query rows against a full prefill, and the full prefill's Sparsity(A, eps). Both attentions of
+    the deviation run through cb_hkvd_attention (the same kernel for the same launch size), so the
+    deviation holds only what the blend changes: zero at r = 100%. Times the diagnostics of one
+    ratio: both encodes, the two attentions, the two passes of the sparsity count and the
+    reductions."""
     import dataclasses
 
     import torch
@@ -863,7 +865,7 @@ def run_diagnostics(args, cfg):
     pos = torch.arange(n, dtype=torch.int32, device=dev)
     k_full = torch.empty((n, cfg.hkv, d), dtype=torch.bfloat16, device=dev)
     q_all = torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev)
-    o_full, o_fused = torch.empty_like(q_all), torch.empty_like(q_all)
+    o_full, o_fused, o_count = torch.empty_like(q_all), torch.empty_like(q_all), torch.empty_like(q_all)
     stats = torch.empty((n, hq, 2), dtype=torch.float32, device=dev)
     counts = torch.empty((n, hq), dtype=torch.int32, device=dev)
     total = torch.empty(1, dtype=torch.int64, device=dev)
@@ -878,7 +880,8 @@ def run_diagnostics(args, cfg):
             cb.cb_rope_rerotate(plan, k_full, t["k_new"], pos, stream=stream)
             cb.cb_rope_rerotate(plan, q_all, t["q"], pos, stream=stream)
             cb.cb_hkvd_attention(plan, q_all, pos, n, bufs.k_fused, bufs.v_fused, n, o_fused, stream=stream)
-            cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_full, stats, counts,
+            cb.cb_hkvd_attention(plan, q_all, pos, n, k_full, t["v_new"], n, o_full, stream=stream)
+            cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_count, stats, counts,
                                      total, stream=stream)
             cb.cb_output_deviation(plan, o_fused, o_full, n, sums, stream=stream)
 
@@ -903,7 +906,7 @@ def run_diagnostics(args, cfg):
                 diag()
             gc = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gc, stream=stream):
-                cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_full, stats,
+                cb.cb_attention_sparsity(plan, q_all, pos, n, k_full, t["v_new"], n, args.eps, o_count, stats,
                                          counts, total, stream=stream)
             start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]
