@@ -22,14 +22,14 @@
 // warpgroups' exponentials (the MUFU pipe) take turns instead of competing.
 //
 // Roles (384 threads):
-//   WG0, WG1 (warps 0-7)  softmax of query tile 0 / 1 (TMEM lane = row); 200 registers each
+//   WG0, WG1 (warps 0-7)  softmax of query tile 0 / 1 (TMEM lane = row); 224 registers each
 //                         (setmaxnreg), since a row's 128 scores are held at once
 //   warp 8   initialises the barriers, requests Q_0, Q_1, K_0 and V_0 at entry, then produces
 //            the K ring (2 stages; stage j % 2 is refilled once S_1(j) is complete)
 //   warp 9   the MMA issuer (one elected lane; tcgen05.mma kind::f16, bf16 in, fp32 accumulate)
 //   warp 10  produces the V ring (2 stages; refilled once P_1(j) V_j is complete)
 //   warp 11  the issuer's waiter: polls the TMA barriers a round needs and publishes them
-// WG2 (warps 8-11) runs with 88 registers (setmaxnreg). Issuer, waiter and WG0 meet on named
+// WG2 (warps 8-11) runs with 56 registers (setmaxnreg). Issuer, waiter and WG0 meet on named
 // barrier 3 once per key tile (WG0's P_0(j) is in TMEM), issuer and WG1 on named barrier 4.
 // TMEM columns: S_0 at 0, S_1 at 128 (fp32, 128 keys); P_i(j) (bf16 pairs, 64 columns) is written
 // over the first half of S_i(j) once it has been read; O_0 at 256, O_1 at 256 + D.

@@ -424,10 +424,11 @@ def test_paired_tile_attention_sparse_rows(cb, hq, hkv, mq, n_keys):
 
 def test_paired_tile_attention_score_jumps(cb):
     # The paired-tile kernel runs a row's later key tiles against its running reference and
-    # takes the tile max only when the tile's P sum passes its limit. Keys whose scores exceed
-    # everything before them by far more than 2^64 (base-2 units of the scaled score), in the
-    # first and second half of odd and even key tiles, make that sum overflow: the tile must be
-    # redone against a moved reference, with O rescaled.
+    # takes a max only when a half tile's P sum passes its limit. Keys whose scores exceed
+    # everything before them by far more than 2^32 (base-2 units of the scaled score), in the
+    # first and second half of odd and even key tiles, make that sum overflow: a first half is
+    # redone before the issuer is told, a second half after the first half of P V has completed,
+    # both against a moved reference with O rescaled.
     hq, hkv, d, n_keys, mq = 32, 8, 128, 4000, 2500
     cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
                               chunk_len=n_keys - 1, n_suffix=1)
@@ -437,10 +438,14 @@ def test_paired_tile_attention_score_jumps(cb):
     q_pos = np.sort(rng.choice(n_keys, size=mq, replace=False))
     q = f32_to_bf16_bits((1.0 + 0.1 * rng.standard_normal((mq, hq, d))).astype(np.float32))
     kf = rng.standard_normal((n_keys, hkv, d)).astype(np.float32)
-    kf[300] = 6.0    # tile 2, second half
-    kf[1410] = 8.0   # tile 11, first half
-    kf[2705] = 12.0  # tile 21, second half
-    kf[3350] = 12.5  # tile 26, first half
+    # each spike passes the previous one by about 2^33 or more; key % 128 < 64 is a tile's first half
+    spikes = {356: 4.0,    # tile 2, second half
+              1410: 6.0,   # tile 11, first half
+              1734: 8.0,   # tile 13, second half
+              2705: 10.0,  # tile 21, first half
+              3440: 12.0}  # tile 26, second half
+    for key, val in spikes.items():
+        kf[key] = val
     k = f32_to_bf16_bits(kf)
     v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
     out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -449,7 +454,7 @@ def test_paired_tile_attention_score_jumps(cb):
     got = bf16_bits_to_f64(bf16_bits(out))
     assert np.all(np.isfinite(got))
     # rows on both sides of every spike, plus seeded rows
-    near = [np.searchsorted(q_pos, t) + o for t in (300, 1410, 2705, 3350) for o in (-1, 0, 1)]
+    near = [np.searchsorted(q_pos, t) + o for t in spikes for o in (-1, 0, 1)]
     pick = np.unique(np.clip(np.concatenate([near, [0, mq - 1], rng.choice(mq, size=160, replace=False)]), 0, mq - 1))
     ref = causal_gqa_attention(bf16_bits_to_f64(q[pick]), q_pos[pick], bf16_bits_to_f64(k), bf16_bits_to_f64(v))
     plan.close()
