@@ -352,7 +352,7 @@ cb_status cb_hkvd_select_noalloc(const void* v_new, const void* v_old, const int
  * layer's attention) of mq query rows runs on the plan's device: 1 for the
  * paired-tile kernel (two 128-row query tiles per CTA whose softmax and
  * tensor-core work alternate; head_dim 128, and only when the launch fills
- * at least two waves of the GPU's SMs), 0 for the one-tile kernel. Both
+ * at least 1.5 waves of the GPU's SMs), 0 for the one-tile kernel. Both
  * compute the same attention; the answer is for profiling and tests. */
 int32_t cb_attention_uses_paired_tiles(const cb_plan* plan, int32_t mq);
 

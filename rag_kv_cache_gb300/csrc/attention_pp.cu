@@ -554,7 +554,10 @@ bool attention_pp_eligible(int32_t mq, int32_t hq, int32_t hkv, int32_t head_dim
     else
       return false;
   }
-  return ctas >= 2 * (int64_t)sms;  // at least two waves: below that one tile per CTA fills more SMs
+  // At least 1.5 waves of its 256-row CTAs. Measured crossovers: at 1.79 waves (the Llama-70B shape's
+  // later layers) the paired kernel runs the layer in 126.5 against 132.8 us; at 1.11 (the ratio
+  // sweep at 15%) it loses, 111.1 against 82.4 us, since one tile per CTA then fills more SMs.
+  return 2 * ctas >= 3 * (int64_t)sms;
 }
 
 cudaError_t launch_hkvd_attention_pp(const void* q, QueryPositions qp, int32_t mq, const void* k, const void* v,
