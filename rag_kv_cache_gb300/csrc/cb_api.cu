@@ -556,13 +556,15 @@ static cb_status enqueue_stage(cb_plan* plan, int32_t layer, const cb_layer_io* 
                          "top-k");
     case CB_STAGE_FUSE: {
       // One launch: the fused cache and the query encoding (both read the layer's selection list).
+      // Small blocks on the layers whose attention runs the paired-tile kernel (see the fuse kernel).
       const bool copy_out = !sh.selects && sh.k > 0;
+      const bool narrow = cb::attention_pp_eligible(sh.mq, c.hq, c.hkv, c.head_dim);
       return cuda_status(cb::launch_blend_fuse(io->k_fused, io->v_fused, io->k_old, io->v_old, io->k_new, io->v_new,
                                                sel, sh.k, copy_out ? io->sel_tok : nullptr,
                                                copy_out ? io->sel_row : nullptr, plan->n_ctx, c.chunk_len,
                                                plan->n_tokens, c.hkv, c.head_dim, c.rope_style, table(plan),
                                                sh.mq > 0 ? io->q : nullptr, sh.mq > 0 ? io->q_rot : nullptr, sh.mq,
-                                               c.hq, plan->err, s),
+                                               c.hq, narrow, plan->err, s),
                          "fuse");
     }
     case CB_STAGE_ATTENTION: {

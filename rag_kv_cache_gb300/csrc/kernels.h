@@ -68,12 +68,13 @@ cudaError_t launch_fuse_scatter(void* k_fused, void* v_fused, const void* k_new,
 // list sel_tok[0..k) is also copied to copy_tok / copy_row (= 0..k-1). With q set,
 // the same launch also encodes the layer's mq query rows (row t < k is token
 // sel_tok[t], row t >= k is token n_ctx + t - k; hq heads each) from the
-// token-indexed q into the compact q_rot.
+// token-indexed q into the compact q_rot. narrow: 2-row blocks (else 8-row blocks).
 cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, const void* v_old,
                               const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
                               int32_t* copy_tok, int32_t* copy_row, int32_t n_ctx, int32_t chunk_len,
                               int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
-                              const void* q, void* q_rot, int32_t mq, int32_t hq, int32_t* err, cudaStream_t s);
+                              const void* q, void* q_rot, int32_t mq, int32_t hq, bool narrow, int32_t* err,
+                              cudaStream_t s);
 
 
 // Positions of the compact query rows: row t < k sits at idx[t], row t >= k at base + (t - k).

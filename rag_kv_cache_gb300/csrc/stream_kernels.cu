@@ -503,9 +503,15 @@ __global__ void __launch_bounds__(kTopkThreads) hkvd_topk_batch_kernel(const __g
 }
 
 // ---------------------------------------------------------------------------
-// Fused cache: 8 consecutive rows per block, one warp per row.
-constexpr int kFuseRows = 8;
-constexpr int kFuseThreads = 256;
+// Fused cache: kFuseRows consecutive rows per block, one warp per row, at most 64 registers a
+// thread. On the large layers whose attention runs the paired-tile kernel the pass uses 2-row
+// blocks: four times the blocks stream the layer faster (the long-context request's fuse in 55.4
+// against 57.7 us, 0.958 against 0.921 of the copy bandwidth), and none of them can sit beside a
+// paired-tile CTA, which holds all of an SM's registers. Beside the one-tile kernel, which leaves
+// room for fuse blocks, the 8-row blocks stay: 2-row blocks there slowed the Mistral-7B step by 9%.
+constexpr int kFuseRowsWide = 8;
+constexpr int kFuseRowsNarrow = 2;
+constexpr int kFuseThreads = 256;  // the standalone scatter
 constexpr int kQParts = 4;  // warps per query row in the fused pass
 
 // First index j in the ascending list sel[0..k) with sel[j] >= key (k if none),
@@ -532,8 +538,8 @@ __device__ __forceinline__ int warp_lower_bound(const int32_t* sel, int k, int k
 // Blocks [0, ceil(n_tokens / 8)) build the fused K/V rows; the blocks after them
 // encode the query rows (one warp per row), so the layer's streaming work is
 // one launch.
-template <int STYLE>
-__global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
+template <int STYLE, int kFuseRows>
+__global__ void __maxnreg__(64) blend_fuse_kernel(
     uint8_t* k_fused, uint8_t* v_fused, const uint8_t* k_old, const uint8_t* v_old, const uint8_t* k_new,
     const uint8_t* v_new, const int32_t* sel, int k, int32_t* out_tok, int32_t* out_row, int n_ctx,
     int chunk_len, int n_tokens, int hkv, int head_dim, RopeTable t, const uint8_t* q, uint8_t* q_rot, int mq,
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kFuseThreads) blend_fuse_kernel(
     const int j0 = warp_lower_bound(sel, k, r0, lane);
     if (lane < kFuseRows) {
       is_sel[lane] = 0;
-      __syncwarp(0xffu);
+      __syncwarp((1u << kFuseRows) - 1);
       const int j = j0 + lane;
       if (j < k) {
         const int tk = sel[j];
@@ -774,23 +780,22 @@ cudaError_t launch_blend_fuse(void* k_fused, void* v_fused, const void* k_old, c
                               const void* k_new, const void* v_new, const int32_t* sel_tok, int32_t k,
                               int32_t* copy_tok, int32_t* copy_row, int32_t n_ctx, int32_t chunk_len,
                               int32_t n_tokens, int32_t hkv, int32_t head_dim, int32_t style, RopeTable t,
-                              const void* q, void* q_rot, int32_t mq, int32_t hq, int32_t* err, cudaStream_t s) {
+                              const void* q, void* q_rot, int32_t mq, int32_t hq, bool narrow, int32_t* err,
+                              cudaStream_t s) {
   if (n_tokens <= 0) return cudaSuccess;
   if (q == nullptr || q_rot == nullptr) mq = 0;
-  const int grid = (n_tokens + kFuseRows - 1) / kFuseRows + (mq * kQParts + kFuseRows - 1) / kFuseRows;
+  const int rows = narrow ? kFuseRowsNarrow : kFuseRowsWide;
+  const int grid = (n_tokens + rows - 1) / rows + (mq * kQParts + rows - 1) / rows;
   auto* kf = (uint8_t*)k_fused;
   auto* vf = (uint8_t*)v_fused;
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, grid, rows * kWarp, 0, s, kf, vf, (const uint8_t*)k_old, (const uint8_t*)v_old,
+                      (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok, copy_row, n_ctx, chunk_len,
+                      n_tokens, hkv, head_dim, t, (const uint8_t*)q, (uint8_t*)q_rot, mq, hq, err);
+  };
   if (style == 0)
-    return launch_pdl(blend_fuse_kernel<0>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
-                      (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
-                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, (const uint8_t*)q, (uint8_t*)q_rot, mq,
-                      hq, err);
-  else
-    return launch_pdl(blend_fuse_kernel<1>, grid, kFuseThreads, 0, s, kf, vf, (const uint8_t*)k_old,
-                      (const uint8_t*)v_old, (const uint8_t*)k_new, (const uint8_t*)v_new, sel_tok, k, copy_tok,
-                      copy_row, n_ctx, chunk_len, n_tokens, hkv, head_dim, t, (const uint8_t*)q, (uint8_t*)q_rot, mq,
-                      hq, err);
-  return cudaPeekAtLastError();
+    return narrow ? go(blend_fuse_kernel<0, kFuseRowsNarrow>) : go(blend_fuse_kernel<0, kFuseRowsWide>);
+  return narrow ? go(blend_fuse_kernel<1, kFuseRowsNarrow>) : go(blend_fuse_kernel<1, kFuseRowsWide>);
 }
 
 
