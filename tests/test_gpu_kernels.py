@@ -422,6 +422,44 @@ def test_paired_tile_attention_sparse_rows(cb, hq, hkv, mq, n_keys):
     assert_close_bf16(got, ref, what=f"paired-tile attention hq={hq} hkv={hkv} mq={mq}")
 
 
+@pytest.mark.parametrize("hq,hkv,mq,n_keys,paired", [(32, 8, 2500, 4000, True), (8, 2, 120, 1500, False)])
+def test_attention_moderate_score_jumps(cb, hq, hkv, mq, n_keys, paired):
+    # Later key tiles whose max passes a row's first-tile max by 2^9 - 2^15 (base-2 units of the
+    # scaled score): below the P-sum limit, so the kernels keep the reference and P reaches
+    # 2^9 - 2^15 unrescaled (the old rule rescaled at 2^8). One spike key per half tile.
+    d = 128
+    cfg = dataclasses.replace(get_config("tiny"), hq=hq, hkv=hkv, head_dim=d, n_chunks=1,
+                              chunk_len=n_keys - 1, n_suffix=1)
+    plan = _plan(cb, cfg)
+    assert bool(cb.cb_attention_uses_paired_tiles(plan, mq)) == paired
+    rng = np.random.default_rng(51 + mq)
+    q_pos = np.sort(rng.choice(np.arange(128, n_keys), size=mq, replace=False))  # every row sees tile 0 whole
+    q = f32_to_bf16_bits((1.0 + 0.1 * rng.standard_normal((mq, hq, d))).astype(np.float32))
+    kf = (0.25 * rng.standard_normal((n_keys, hkv, d))).astype(np.float32)
+    spikes = [k for k in range(160, n_keys, 128)] + [k for k in range(230, n_keys, 256)]
+    kf[spikes] = rng.uniform(0.72, 0.90, size=(len(spikes), 1, 1)).astype(np.float32)
+    k = f32_to_bf16_bits(kf)
+    v = f32_to_bf16_bits(rng.standard_normal((n_keys, hkv, d)).astype(np.float32))
+    # the regime holds: for every query row, spike keys it sees score 2^9 - 2^15 above its tile-0 max
+    qd, kd = bf16_bits_to_f64(q), bf16_bits_to_f64(k)
+    c = np.log2(np.e) / np.sqrt(d)
+    g = hq // hkv
+    s0 = np.einsum("qhd,khd->qhk", qd, kd[:128].repeat(g, axis=1)).max(axis=2) * c
+    ss = np.einsum("qhd,khd->qhk", qd, kd[spikes].repeat(g, axis=1)) * c
+    jump = ss - s0[:, :, None]
+    seen = np.asarray(spikes)[None, :] <= q_pos[:, None]
+    assert seen.any()
+    assert np.all((jump[seen.nonzero()[0], :, seen.nonzero()[1]] > 9) & (jump[seen.nonzero()[0], :, seen.nonzero()[1]] < 15))
+    out = torch.full((mq, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cb.cb_hkvd_attention(plan, bf16_tensor(q), _i32(q_pos), mq, bf16_tensor(k), bf16_tensor(v), n_keys, out)
+    plan.check()
+    got = bf16_bits_to_f64(bf16_bits(out))
+    pick = np.unique(np.concatenate([[0, mq - 1], rng.choice(mq, size=min(mq, 160), replace=False)]))
+    ref = causal_gqa_attention(qd[pick], q_pos[pick], kd, bf16_bits_to_f64(v))
+    plan.close()
+    assert_close_bf16(got[pick], ref, what=f"attention with moderate score jumps ({'paired' if paired else 'one-tile'})")
+
+
 def test_paired_tile_attention_score_jumps(cb):
     # The paired-tile kernel runs a row's later key tiles against its running reference and
     # takes a max only when a half tile's P sum passes its limit. Keys whose scores exceed
