@@ -372,6 +372,17 @@ __global__ void __launch_bounds__(kTThreads, 1)
   __syncthreads();
   if (merged && s_last) {
     __threadfence();
+    // The partial O rows of this thread's first output group go out first, so that their round trip
+    // to L2 overlaps the one of the weights below (up to kMergeBatch splits per batch of loads).
+    constexpr int kMergeBatch = 8;
+    const int n_groups = p.G * D / 4;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + (size_t)g * n_split * p.G * D);
+    float4 first[kMergeBatch];
+    if ((int)threadIdx.x < n_groups) {
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u)
+        if (u < n_split) first[u] = __ldcg(src + (size_t)u * n_groups + threadIdx.x);
+    }
     // merge weights [split][head] in the K ring, free now (every load landed, every MMA completed)
     float(*s_w)[kTMaxG] = reinterpret_cast<float(*)[kTMaxG]>(smem_raw + (sK0 - smem_u32(smem_raw)));
     // weights: warp w takes heads w, w + 8, ...; lane l the splits l and l + 32
@@ -392,19 +403,23 @@ __global__ void __launch_bounds__(kTThreads, 1)
       if (lane + 32 < n_split) s_w[lane + 32][h] = wc * inv;
     }
     __syncthreads();
-    // outputs in float4 groups, each thread summing the splits of its groups with all loads issued first
-    const int n_groups = p.G * D / 4;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + (size_t)g * n_split * p.G * D);
+    // outputs in float4 groups, each thread summing the splits of its groups with a batch of loads
+    // in flight at a time
     for (int grp = threadIdx.x; grp < n_groups; grp += kTThreads) {
       const int h = (grp * 4) / D;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < n_split; s0 += 8) {
-        float4 t4[8];
+      for (int s0 = 0; s0 < n_split; s0 += kMergeBatch) {
+        float4 t4[kMergeBatch];
+        if (s0 == 0 && grp == (int)threadIdx.x) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (s0 + u < n_split) t4[u] = __ldcg(src + (size_t)(s0 + u) * n_groups + grp);
+          for (int u = 0; u < kMergeBatch; ++u) t4[u] = first[u];
+        } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < kMergeBatch; ++u)
+            if (s0 + u < n_split) t4[u] = __ldcg(src + (size_t)(s0 + u) * n_groups + grp);
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
           if (s0 + u < n_split) {
             const float w = s_w[s0 + u][h];
             acc.x = fmaf(w, t4[u].x, acc.x);
