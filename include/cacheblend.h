@@ -243,8 +243,10 @@ cb_status cb_decode_attention(cb_plan* plan, const void* q, const void* k, const
  * counts the weights below eps of every query row and head over all n_keys keys:
  *   counts[i * hq + h] = |{j < n_keys: A[h]_ij < eps}|,  *total = sum of counts (uint64).
  * Two launches of the attention kernel: the first writes out (as cb_hkvd_attention) and
- * row_stats ([mq, hq] float2, the softmax's (max, sum) in log2 units), the second recomputes the
- * same scores and compares them with max + log2(eps * sum); then a reduction writes *total.
+ * row_stats ([mq, hq] float2: a reference r in log2 units and the sum s of 2^(score - r), so
+ * that the row's softmax denominator is s * 2^r; r lies at most 16 below the row's largest
+ * scaled score), the second recomputes the same scores and compares them with r + log2(eps * s);
+ * then a reduction writes *total.
  * Sparsity = total / (hq * mq * n_keys) (with q_pos = 0 .. n - 1 and n_keys = n this is the
  * page's n x n figure summed over heads). eps must be positive. Weights within about 1e-5 of eps
  * (relative) may fall on either side of it (fp32 scores and softmax sums). */
