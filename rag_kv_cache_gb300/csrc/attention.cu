@@ -115,8 +115,9 @@ struct Params {
   float scale_log2;
   uint8_t* out;
   int32_t* err;
-  // Diagnostics (null in the blend): row_stats receives each row's (max, sum) of the softmax in
-  // log2 units, A_ij = 2^(s_ij * scale_log2 - max) / sum. The counting instance reads count_stats
+  // Diagnostics (null in the blend): row_stats receives each row's (reference, sum) of the softmax
+  // in log2 units, A_ij = 2^(s_ij * scale_log2 - reference) / sum (the reference is the softmax's
+  // own, at most 16 below the row's max). The counting instance reads count_stats
   // (such a pair per row) and writes to counts, per row, how many of the n_keys weights lie
   // below 2^log2_eps (masked keys, weight 0, included).
   float2* row_stats;
